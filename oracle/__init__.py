@@ -1,0 +1,248 @@
+"""CPU oracle for the fused decode-seam operators -- TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``edge_oracle.c`` (plain C, fp64 scalar loops, no
+fast-math).  This module compiles it with the host C compiler and wraps it with
+ctypes over numpy arrays.  It shares no code with the CUDA library and never
+imports it.  Only the tests, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg may use it; the product path never does.
+
+Arrays hold raw element storage: ``float32`` for binary32, ``uint16`` for
+binary16 and bfloat16, ``uint8`` for E4M3 codes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+
+import numpy as np
+
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
+ROTATE_HALF, INTERLEAVED = 0, 1
+SILU, GELU_TANH = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "edge_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB = None
+
+STORAGE = {F32: np.float32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8}
+
+
+def lib_path() -> str:
+    return os.path.join(_OUT_DIR, f"liboracle_{platform.machine()}.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle for this host (x86_64 here, aarch64 on the GPU host)."""
+    out = lib_path()
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = [os.environ.get("CC", "cc"), "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        L = ctypes.CDLL(build())
+        P, I64, I, F, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
+        L.oracle_round.argtypes = [D, I]
+        L.oracle_round.restype = D
+        L.oracle_bits.argtypes = [D, I]
+        L.oracle_bits.restype = ctypes.c_uint32
+        L.oracle_value.argtypes = [ctypes.c_uint32, I]
+        L.oracle_value.restype = D
+        L.oracle_decode_array.argtypes = [P, I, I64, P]
+        L.oracle_encode_array.argtypes = [P, I64, I, P]
+        L.oracle_quantize_array.argtypes = [P, I64, F, P]
+        L.oracle_rmsnorm.argtypes = [P, I, P, P, P, I, I64, I64, F, I, F]
+        L.oracle_add_rmsnorm.argtypes = [P, I, P, P, P, P, P, I, I64, I64, F, I, F]
+        L.oracle_glu_act.argtypes = [P, I, P, P, I, I64, I64, I, F]
+        L.oracle_rope.argtypes = [P, I, P, I, I64, I, I, I, I, P, P, P, I64]
+        L.oracle_qk_norm_rope.argtypes = [P, P, I, P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I,
+                                          I, I, P, P, P, I64, F, I, F, D]
+        L.oracle_set_rotation_scale.argtypes = [D]
+        for name in ("oracle_rmsnorm", "oracle_add_rmsnorm", "oracle_glu_act", "oracle_rope",
+                     "oracle_qk_norm_rope", "oracle_version"):
+            getattr(L, name).restype = ctypes.c_int
+        _LIB = L
+    return _LIB
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype=None):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if dtype is not None and a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what}: invalid arguments (rc={rc})")
+
+
+# ---------------------------------------------------------------- formats
+
+def round_to(v, fmt: int) -> float:
+    """Round one fp64 value to ``fmt`` (nearest, ties to even)."""
+    return _lib().oracle_round(float(v), fmt)
+
+
+def bits_of(v, fmt: int) -> int:
+    return int(_lib().oracle_bits(float(v), fmt))
+
+
+def value_of(bits: int, fmt: int) -> float:
+    return _lib().oracle_value(int(bits), fmt)
+
+
+def decode(a: np.ndarray, fmt: int) -> np.ndarray:
+    """Raw element storage -> fp64 values."""
+    a = _c(a, STORAGE[fmt])
+    out = np.empty(a.shape, np.float64)
+    _lib().oracle_decode_array(_ptr(a), fmt, a.size, _ptr(out))
+    return out
+
+
+def encode(v: np.ndarray, fmt: int) -> np.ndarray:
+    """fp64 values -> raw storage of their rounding to ``fmt``."""
+    v = _c(np.asarray(v, np.float64))
+    out = np.empty(v.shape, STORAGE[fmt])
+    _lib().oracle_encode_array(_ptr(v), v.size, fmt, _ptr(out))
+    return out
+
+
+def quantize(v: np.ndarray, inv_scale: float) -> np.ndarray:
+    """Exact values -> the E4M3 codes the FP8 epilogue emits for them."""
+    v = _c(np.asarray(v, np.float64))
+    out = np.empty(v.shape, np.uint8)
+    _lib().oracle_quantize_array(_ptr(v), v.size, ctypes.c_float(inv_scale), _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- ops
+
+def rmsnorm(x, w, fmt, eps, weight_offset=0, out_fmt=None, inv_scale=1.0):
+    """x: [rows, hidden] storage.  Returns (out storage, exact pre-rounding values)."""
+    out_fmt = fmt if out_fmt is None else out_fmt
+    x = _c(x, STORAGE[fmt])
+    w = _c(w, STORAGE[fmt])
+    rows, hidden = x.shape
+    out = np.empty(x.shape, STORAGE[out_fmt])
+    pre = np.empty(x.shape, np.float64)
+    rc = _lib().oracle_rmsnorm(_ptr(out), out_fmt, _ptr(pre), _ptr(x), _ptr(w), fmt, rows, hidden,
+                               eps, weight_offset, inv_scale)
+    _check(rc, "rmsnorm")
+    return out, pre
+
+
+def add_rmsnorm(x, residual, w, fmt, eps, weight_offset=0, out_fmt=None, inv_scale=1.0):
+    """Returns (out storage, new residual storage, exact pre-rounding values)."""
+    out_fmt = fmt if out_fmt is None else out_fmt
+    x = _c(x, STORAGE[fmt])
+    residual = _c(residual, STORAGE[fmt])
+    w = _c(w, STORAGE[fmt])
+    rows, hidden = x.shape
+    out = np.empty(x.shape, STORAGE[out_fmt])
+    res = np.empty(x.shape, STORAGE[fmt])
+    pre = np.empty(x.shape, np.float64)
+    rc = _lib().oracle_add_rmsnorm(_ptr(out), out_fmt, _ptr(pre), _ptr(res), _ptr(x),
+                                   _ptr(residual), _ptr(w), fmt, rows, hidden, eps, weight_offset,
+                                   inv_scale)
+    _check(rc, "add_rmsnorm")
+    return out, res, pre
+
+
+def glu_act(gate_up, fmt, act, out_fmt=None, inv_scale=1.0):
+    """gate_up: [rows, 2d] storage (gate first).  Returns (out storage, exact values)."""
+    out_fmt = fmt if out_fmt is None else out_fmt
+    gate_up = _c(gate_up, STORAGE[fmt])
+    rows, two_d = gate_up.shape
+    d = two_d // 2
+    out = np.empty((rows, d), STORAGE[out_fmt])
+    pre = np.empty((rows, d), np.float64)
+    rc = _lib().oracle_glu_act(_ptr(out), out_fmt, _ptr(pre), _ptr(gate_up), fmt, rows, d, act,
+                               inv_scale)
+    _check(rc, "glu_act")
+    return out, pre
+
+
+def rope(x, fmt, rotary_dim, layout, positions, cos, sin, out_fmt=None):
+    """Standalone rotary embedding of x: [tokens, heads, head_dim] storage."""
+    out_fmt = fmt if out_fmt is None else out_fmt
+    x = _c(x, STORAGE[fmt])
+    tokens, heads, head_dim = x.shape
+    positions = _c(np.asarray(positions, np.int64))
+    cos = _c(cos, np.float32)
+    sin = _c(sin, np.float32)
+    cache_len = 0 if cos is None else cos.shape[0]
+    out = np.empty(x.shape, STORAGE[out_fmt])
+    rc = _lib().oracle_rope(_ptr(out), out_fmt, _ptr(x), fmt, tokens, heads, head_dim, rotary_dim,
+                            layout, _ptr(positions), _ptr(cos), _ptr(sin), cache_len)
+    _check(rc, "rope")
+    return out
+
+
+class QKResult:
+    """Outputs of the fused prologue plus the tie-policy diagnostics."""
+
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def qk_norm_rope(q, k, wq, wk, fmt, rotary_dim, layout, positions, cos, sin, eps,
+                 weight_offset=0, out_fmt=None, inv_scale=1.0, eta=2.0 ** -20, cache_len=None):
+    """q: [T, Hq, D], k: [T, Hk, D] storage; cos/sin: [P, rotary_dim/2] fp32."""
+    out_fmt = fmt if out_fmt is None else out_fmt
+    q = _c(q, STORAGE[fmt])
+    k = _c(k, STORAGE[fmt])
+    wq = _c(wq, STORAGE[fmt])
+    wk = _c(wk, STORAGE[fmt])
+    T, Hq, D = q.shape
+    Hk = k.shape[1]
+    positions = _c(np.asarray(positions, np.int64))
+    cos = _c(cos, np.float32)
+    sin = _c(sin, np.float32)
+    if cache_len is None:
+        cache_len = 0 if cos is None else cos.shape[0]
+    res = QKResult(
+        q_out=np.empty(q.shape, STORAGE[out_fmt]), k_out=np.empty(k.shape, STORAGE[out_fmt]),
+        q_pre=np.empty(q.shape), k_pre=np.empty(k.shape),
+        q_alt=np.empty(q.shape), k_alt=np.empty(k.shape),
+        q_mag=np.empty(q.shape), k_mag=np.empty(k.shape))
+    rc = _lib().oracle_qk_norm_rope(
+        _ptr(res.q_out), _ptr(res.k_out), out_fmt, _ptr(res.q_pre), _ptr(res.k_pre),
+        _ptr(res.q_alt), _ptr(res.k_alt), _ptr(res.q_mag), _ptr(res.k_mag), _ptr(q), _ptr(k),
+        _ptr(wq), _ptr(wk), fmt, T, Hq, Hk, D, rotary_dim, layout, _ptr(positions), _ptr(cos),
+        _ptr(sin), cache_len, eps, weight_offset, inv_scale, eta)
+    _check(rc, "qk_norm_rope")
+    return res
+
+
+class rotation_scale:
+    """Context manager that plants a factor into the oracle's rotation (the
+    strength control of the ninfer text-profile pull request, "Output")."""
+
+    def __init__(self, s: float):
+        self.s = s
+
+    def __enter__(self):
+        _lib().oracle_set_rotation_scale(self.s)
+        return self
+
+    def __exit__(self, *exc):
+        _lib().oracle_set_rotation_scale(1.0)
+        return False

@@ -1,0 +1,94 @@
+"""Shared test helpers: dtype plumbing and the parity acceptance rules.
+
+Acceptance rules (the GPU computes in fp32, the oracle in fp64):
+
+* integer-like results (residual sums) are compared bit for bit;
+* bf16/fp16 outputs must lie within 1 ulp of the oracle's rounded value;
+* the strict check additionally requires every output to be a correct
+  rounding of some value within ``eta * mag`` of the oracle's exact value
+  ``pre`` (or of its alternate ``alt``, when an intermediate rounding was at
+  a near tie).  That is bit-exactness except near rounding boundaries, with a
+  band ``eta`` derived from the fp32 error of the kernel;
+* FP8 codes are held to the strict check (bit-exact outside the band);
+* fp32 outputs must satisfy |y - pre| <= rel * mag (+ a tiny absolute floor).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+TORCH_FMT = {torch.float32: oracle.F32, torch.float16: oracle.F16, torch.bfloat16: oracle.BF16}
+
+
+def storage(t: torch.Tensor) -> np.ndarray:
+    """Raw element storage of a CPU tensor, as the oracle takes it."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return t.view(torch.uint8).numpy()
+    raise TypeError(t.dtype)
+
+
+def ordered(bits: np.ndarray, fmt: int) -> np.ndarray:
+    """Map bit patterns to integers whose order is the value order (for ulp distances)."""
+    if fmt == oracle.F32:
+        b = bits.view(np.uint32).astype(np.int64)
+        sign = b >> 31
+        mag = b & 0x7FFFFFFF
+    elif fmt == oracle.E4M3:
+        b = bits.astype(np.int64)
+        sign = b >> 7
+        mag = b & 0x7F
+    else:
+        b = bits.astype(np.int64)
+        sign = b >> 15
+        mag = b & 0x7FFF
+    return np.where(sign == 1, -mag, mag)
+
+
+def ulp_distance(a: np.ndarray, b: np.ndarray, fmt: int) -> np.ndarray:
+    return np.abs(ordered(a, fmt) - ordered(b, fmt))
+
+
+def _round_codes(v: np.ndarray, out_fmt: int, inv_scale: float) -> np.ndarray:
+    if out_fmt == oracle.E4M3:
+        return oracle.quantize(v, inv_scale)
+    return oracle.encode(v, out_fmt)
+
+
+def strict_ok(got: np.ndarray, pre: np.ndarray, mag: np.ndarray, out_fmt: int, eta: float,
+              inv_scale: float = 1.0, alt: np.ndarray | None = None) -> np.ndarray:
+    """Per element: got is the rounding of some value in [pre - eta*mag, pre + eta*mag]
+    (rounding is monotone, so it suffices to bracket the two ends)."""
+    got_o = ordered(got, out_fmt)
+
+    def inside(center):
+        lo = _round_codes(center - eta * mag, out_fmt, inv_scale)
+        hi = _round_codes(center + eta * mag, out_fmt, inv_scale)
+        lo_o, hi_o = ordered(lo, out_fmt), ordered(hi, out_fmt)
+        return (got_o >= np.minimum(lo_o, hi_o)) & (got_o <= np.maximum(lo_o, hi_o))
+
+    ok = inside(pre)
+    if alt is not None:
+        has = ~np.isnan(alt)
+        if has.any():
+            ok_alt = np.zeros_like(ok)
+            ok_alt[has] = inside(np.where(has, alt, 0.0))[has]
+            ok |= ok_alt
+    return ok
+
+
+def f32_ok(got: np.ndarray, pre: np.ndarray, mag: np.ndarray, rel: float,
+           floor: float = 1e-30) -> np.ndarray:
+    g = got.view(np.float32).astype(np.float64)
+    return np.abs(g - pre) <= rel * mag + floor
+
+
+def report(name: str, ok: np.ndarray) -> str:
+    bad = np.flatnonzero(~ok.ravel())
+    return f"{name}: {bad.size} of {ok.size} outside tolerance; first at {bad[:8].tolist()}"

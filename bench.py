@@ -1,0 +1,649 @@
+#!/usr/bin/env python3
+"""Decode-seam benchmark: HBM GB/s of the fused ops on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl edge|reference]
+
+Prints one JSON line on rank 0.
+
+Workload (one step).  The seam ops of one decode pass through a 36-layer
+decoder shaped like the decode configuration:
+  - hidden 2560, gate 2 x 9728, 32 query and 8 key heads of head_dim 128;
+  - T = 64 tokens (the largest decode width of that configuration), bf16.
+Per layer, in order:
+    add_rmsnorm(x=mlp_out, residual) -> h1                input norm, direct weight
+    qk_norm_rope(q, k) in place, rotate-half 128 of 128   theta 1e6, cache 4096
+    add_rmsnorm(x=attn_out, residual) -> h2               post-attention norm
+    glu_act(gate_up [T, 2*9728], SiLU) -> act
+Every layer owns its buffers, so one step touches about 277 MB, more than
+the 129 MB L2.  Successive steps therefore read their inputs from HBM, and
+no L2 flush is needed.  The step (144 launches) is captured in one CUDA graph
+and replayed.  `value` is the algorithmic bytes of all ranks' steps divided
+by the slowest rank's device time, in GB/s.
+
+Extra keys:
+  - roofline: the dominant kernel's achieved GB/s over the measured HBM
+    copy peak;
+  - cpu_baseline: the CPU oracle timed on the host;
+  - e2e: host-pinned inputs -> device -> host results, through the same
+    C-ABI calls;
+  - sweep: per-op GB/s vs T, cold L2;
+  - t1_us_per_call: graph-replayed microseconds per call at T=1 with a
+    warm L2, 32 launches per sample.
+
+--impl reference times the CPU oracle instead, on a bounded sample of the
+same workload (8 tokens of one layer per step), on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "QK-norm+RoPE & add-RMSNorm: HBM GB/s (% peak) vs T; µs/call at T=1"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+
+# decode workload geometry
+T_DEC, HID, INTER, HQ, HK, HD, LAYERS = 64, 2560, 9728, 32, 8, 128, 36
+THETA, CACHE, EPS = 1e6, 4096, 1e-6
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["edge", "reference"], default="edge")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- bytes
+
+def bytes_add_rmsnorm(T, H, s=2, out_s=2, weight=True):
+    return T * H * s * 3 + T * H * out_s + (H * s if weight else 0)
+
+
+def bytes_rmsnorm(T, H, s=2, out_s=2, weight=True):
+    return T * H * s + T * H * out_s + (H * s if weight else 0)
+
+
+def bytes_qk(T, Hq, Hk, D, rot, s=2, out_s=2):
+    # q, k read and written; two norm weights; one position and two cache
+    # rows of rot/2 fp32 per token
+    return T * (Hq + Hk) * D * (s + out_s) + 2 * D * s + T * 8 + T * 2 * (rot // 2) * 4
+
+
+def bytes_glu(T, d, s=2, out_s=2):
+    return T * d * 2 * s + T * d * out_s
+
+
+def layer_bytes(T=T_DEC):
+    return (2 * bytes_add_rmsnorm(T, HID) + bytes_qk(T, HQ, HK, HD, HD) + bytes_glu(T, INTER))
+
+
+# ---------------------------------------------------------------- environment
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (50 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1 + 0.06]
+        window = "timed"
+        if not rows:
+            rows = [r for (_, r) in self.rows]
+            window = "run"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows), "window": window,
+                "power_w_max": max((float(r[4]) for r in rows
+                                    if r[4].replace(".", "").isdigit()), default=None)}
+
+
+def visible_index(local_rank):
+    v = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if v:
+        ids = [x.strip() for x in v.split(",")]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_layer_args(T, seed=0):
+    """Storage arrays for one layer of the workload (the oracle's inputs)."""
+    import torch
+
+    import oracle
+    from memory_bound_decode_qk_gb300 import synth
+
+    def st(t):
+        t = t.contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 \
+            else t.numpy()
+
+    r1 = synth.rows_inputs(seed, torch.bfloat16, T, HID)
+    r2 = synth.rows_inputs(seed + 100, torch.bfloat16, T, HID)
+    q = synth.qk_inputs(seed, torch.bfloat16, T, HQ, HK, HD, HD, theta=THETA, cache_len=CACHE,
+                        positions="arange", w_mean=1.0, w_std=0.02)
+    g = synth.glu_inputs(seed, torch.bfloat16, T, INTER)
+    return dict(
+        r1=[st(r1["x"]), st(r1["residual"]), st(r1["w"])],
+        r2=[st(r2["x"]), st(r2["residual"]), st(r2["w"])],
+        qk=[st(q["q"]), st(q["k"]), st(q["wq"]), st(q["wk"])],
+        pos=q["positions"].numpy(), cos=q["cos"].numpy(), sin=q["sin"].numpy(),
+        gu=st(g["gate_up"]), oracle=oracle)
+
+
+def oracle_layer(a):
+    o = a["oracle"]
+    o.add_rmsnorm(*a["r1"], o.BF16, EPS)
+    o.qk_norm_rope(*a["qk"], o.BF16, HD, o.ROTATE_HALF, a["pos"], a["cos"], a["sin"], EPS, 0)
+    o.add_rmsnorm(*a["r2"], o.BF16, EPS)
+    o.glu_act(a["gu"], o.BF16, o.SILU)
+
+
+def cpu_baseline(seconds):
+    a = oracle_layer_args(T_DEC)
+    oracle_layer(a)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_layer(a)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    gbs = layer_bytes() * n / el / 1e9
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of the workload's layers (T={T_DEC}, 4 ops each) in {el:.1f} s, "
+                      f"single-threaded C fp64 oracle on the host"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    T = 8  # bounded sample: 8 tokens of one layer per step
+    a = oracle_layer_args(T)
+    for _ in range(args.warmup):
+        oracle_layer(a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_layer(a)
+    el = time.perf_counter() - t0
+    gbs = layer_bytes(T) * args.steps / el / 1e9
+    sample = f"{T} tokens of one layer (4 ops) per step; single-threaded C fp64 oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode seams of a 36-layer decoder (reference arm: sample)",
+                   "T": T, "hidden": HID, "gate": INTER, "heads": [HQ, HK], "head_dim": HD},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU workload
+
+class Layer:
+    pass
+
+
+def build_layers(torch, synth, device, seed):
+    """Per-layer device buffers; values from one seeded layer, copied into each."""
+    bf = torch.bfloat16
+    r1 = synth.rows_inputs(seed, bf, T_DEC, HID)
+    r2 = synth.rows_inputs(seed + 100, bf, T_DEC, HID)
+    q = synth.qk_inputs(seed, bf, T_DEC, HQ, HK, HD, HD, theta=THETA, cache_len=CACHE,
+                        positions="arange", w_mean=1.0, w_std=0.02)
+    g = synth.glu_inputs(seed, bf, T_DEC, INTER)
+    shared = dict(pos=q["positions"].to(device), cos=q["cos"].to(device),
+                  sin=q["sin"].to(device))
+    layers = []
+    for _ in range(LAYERS):
+        L = Layer()
+        L.mlp_out = r1["x"].to(device)
+        L.res = r1["residual"].to(device)
+        L.w_in = r1["w"].to(device)
+        L.h1 = torch.empty_like(L.mlp_out)
+        L.q = q["q"].to(device)
+        L.k = q["k"].to(device)
+        L.wq = q["wq"].to(device)
+        L.wk = q["wk"].to(device)
+        L.attn_out = r2["x"].to(device)
+        L.w_post = r2["w"].to(device)
+        L.h2 = torch.empty_like(L.attn_out)
+        L.gate_up = g["gate_up"].to(device)
+        L.act = torch.empty(T_DEC, INTER, dtype=bf, device=device)
+        layers.append(L)
+    return layers, shared
+
+
+OPS = ("add_rmsnorm_in", "qk_norm_rope", "add_rmsnorm_post", "glu_silu")
+OP_BYTES = {"add_rmsnorm_in": bytes_add_rmsnorm(T_DEC, HID),
+            "qk_norm_rope": bytes_qk(T_DEC, HQ, HK, HD, HD),
+            "add_rmsnorm_post": bytes_add_rmsnorm(T_DEC, HID),
+            "glu_silu": bytes_glu(T_DEC, INTER)}
+OP_KERNEL = {"add_rmsnorm_in": "rows_vec_kernel", "qk_norm_rope": "qk_vec_kernel",
+             "add_rmsnorm_post": "rows_vec_kernel", "glu_silu": "glu_vec_kernel"}
+OP_SOURCE = {"rows_vec_kernel": "rows.cu", "qk_vec_kernel": "qk_norm_rope.cu",
+             "glu_vec_kernel": "glu.cu"}
+
+
+def layer_ops(ops, L, sh):
+    """The four seam ops of one layer, as (name, thunk) pairs."""
+    return [
+        ("add_rmsnorm_in", lambda: ops.add_rmsnorm(L.mlp_out, L.res, L.w_in, eps=EPS, out=L.h1)),
+        ("qk_norm_rope", lambda: ops.qk_norm_rope(L.q, L.k, L.wq, L.wk, sh["pos"], sh["cos"],
+                                                  sh["sin"], rotary_dim=HD, eps=EPS,
+                                                  weight_offset=0, q_out=L.q, k_out=L.k)),
+        ("add_rmsnorm_post", lambda: ops.add_rmsnorm(L.attn_out, L.res, L.w_post, eps=EPS,
+                                                     out=L.h2)),
+        ("glu_silu", lambda: ops.glu_act(L.gate_up, ops.SILU, out=L.act)),
+    ]
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # eager once (library load, launch checks) before capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def source_sha(kernel):
+    p = os.path.join(ROOT, "memory_bound_decode_qk_gb300", "csrc", OP_SOURCE[kernel])
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get("decode_step", {}).get(kernel)
+    if not e or e.get("source_sha") != source_sha(kernel):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- sweep
+
+def sweep(torch, ops, synth, device, peak):
+    """Per-op device time vs T with a cold L2: an L2-sized write separates
+    every timed launch, and events bracket the launch alone (median of 15)."""
+    bf = torch.bfloat16
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    out = {}
+
+    def time_cold(fn, reps=15):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            fn()
+            for a, b in evs:
+                flush.fill_(1.0)
+                a.record(stream)
+                fn()
+                b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in evs])) * 1e3  # us
+
+    def entry(us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return [round(us, 3), round(gbs, 1), round(gbs / peak, 4)]
+
+    # QK-norm+RoPE, text profile (head_dim 256, rotary 64, out of place)
+    for (hq, hk) in ((16, 2), (24, 4)):
+        key = f"qk_norm_rope_bf16_{hq}x{hk}_d256_r64"
+        out[key] = {}
+        for T in (1, 8, 32, 128, 256, 512, 1024, 2048):
+            i = synth.qk_inputs(0, bf, T, hq, hk, 256, 64, theta=1e7, cache_len=32768,
+                                positions="offset", w_std=0.05)
+            d = {k: v.to(device) for k, v in i.items()}
+            qo, ko = torch.empty_like(d["q"]), torch.empty_like(d["k"])
+            fn = lambda: ops.qk_norm_rope(d["q"], d["k"], d["wq"], d["wk"], d["positions"],
+                                          d["cos"], d["sin"], rotary_dim=64, weight_offset=1,
+                                          q_out=qo, k_out=ko)
+            out[key][str(T)] = entry(time_cold(fn), bytes_qk(T, hq, hk, 256, 64))
+    # residual-add RMSNorm, bf16 out and FP8 out, and the no-weight FP8 RMSNorm
+    for H in (2048, 1024, 2560):
+        for fp8 in (False, True):
+            key = f"add_rmsnorm_bf16_h{H}" + ("_fp8" if fp8 else "")
+            out[key] = {}
+            for T in (1, 16, 64, 256, 512, 1024, 4096):
+                i = synth.rows_inputs(0, bf, T, H)
+                x, r, w = (i[k].to(device) for k in ("x", "residual", "w"))
+                o = torch.empty(T, H, dtype=torch.uint8 if fp8 else bf, device=device)
+                fn = lambda: ops.add_rmsnorm(x, r, w, eps=EPS, out=o, fp8=fp8, inv_scale=40.0)
+                out[key][str(T)] = entry(time_cold(fn), bytes_add_rmsnorm(T, H, out_s=1 if fp8 else 2))
+    key = "rmsnorm_noweight_bf16_h2048_fp8"
+    out[key] = {}
+    for T in (1, 64, 512, 4096):
+        i = synth.rows_inputs(0, bf, T, 2048, residual=False)
+        x = i["x"].to(device)
+        o = torch.empty(T, 2048, dtype=torch.uint8, device=device)
+        fn = lambda: ops.rmsnorm(x, None, eps=EPS, out=o, fp8=True, inv_scale=40.0)
+        out[key][str(T)] = entry(time_cold(fn), bytes_rmsnorm(T, 2048, out_s=1, weight=False))
+    # gates
+    for name, d_, act, fp8 in (("glu_silu_bf16_d9728", INTER, ops.SILU, False),
+                               ("glu_gelu_bf16_d2048_fp8", 2048, ops.GELU_TANH, True)):
+        out[name] = {}
+        for T in (1, 64, 512, 4096):
+            gu = synth.glu_inputs(0, bf, T, d_)["gate_up"].to(device)
+            o = torch.empty(T, d_, dtype=torch.uint8 if fp8 else bf, device=device)
+            fn = lambda: ops.glu_act(gu, act, out=o, fp8=fp8, inv_scale=40.0)
+            out[name][str(T)] = entry(time_cold(fn), bytes_glu(T, d_, out_s=1 if fp8 else 2))
+    del flush
+    return out
+
+
+def t1_latency(torch, ops, synth, device):
+    """Graph replay of 32 back-to-back T=1 calls on the same buffers (warm L2):
+    200 samples after 20 warm-up replays, median and IQR in us per call."""
+    bf = torch.bfloat16
+    stream = torch.cuda.Stream(device)
+    res = {}
+
+    def measure(fn):
+        def many():
+            for _ in range(32):
+                fn()
+        g = capture(torch, many, stream)
+        for _ in range(20):
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(200)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+        torch.cuda.synchronize()
+        per = np.array([a.elapsed_time(b) for a, b in evs]) * 1e3 / 32
+        q1, med, q3 = np.percentile(per, [25, 50, 75])
+        return {"median": round(float(med), 3), "iqr": [round(float(q1), 3), round(float(q3), 3)]}
+
+    for (hq, hk) in ((16, 2), (24, 4)):
+        i = synth.qk_inputs(0, bf, 1, hq, hk, 256, 64, theta=1e7, cache_len=32768,
+                            positions="offset", w_std=0.05)
+        d = {k: v.to(device) for k, v in i.items()}
+        qo, ko = torch.empty_like(d["q"]), torch.empty_like(d["k"])
+        res[f"qk_norm_rope_{hq}x{hk}"] = measure(
+            lambda: ops.qk_norm_rope(d["q"], d["k"], d["wq"], d["wk"], d["positions"], d["cos"],
+                                     d["sin"], rotary_dim=64, weight_offset=1, q_out=qo,
+                                     k_out=ko))
+    i = synth.rows_inputs(0, bf, 1, HID)
+    x, r, w = (i[k].to(device) for k in ("x", "residual", "w"))
+    o = torch.empty_like(x)
+    res["add_rmsnorm_h2560"] = measure(lambda: ops.add_rmsnorm(x, r, w, eps=EPS, out=o))
+    gu = synth.glu_inputs(0, bf, 1, INTER)["gate_up"].to(device)
+    og = torch.empty(1, INTER, dtype=bf, device=device)
+    res["glu_silu_d9728"] = measure(lambda: ops.glu_act(gu, ops.SILU, out=og))
+    return res
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from memory_bound_decode_qk_gb300 import _build, edge_ops as ops, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if not os.path.exists(_build.LIB):
+        if rank == 0:
+            _build.build()
+        if world > 1:
+            dist.barrier()
+    ops.lib()  # loud failure if the CUDA library is missing: no fallback
+    peak, peak_kind = measured_peak()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    layers, sh = build_layers(torch, synth, device, seed=rank)
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for L in layers:
+            for _, fn in layer_ops(ops, L, sh):
+                fn()
+
+    graph = capture(torch, step, stream)
+    launches_per_step = LAYERS * len(OPS)
+    step_bytes = LAYERS * layer_bytes()
+
+    # per-kernel breakdown: the same step with an event between launches
+    marks = []
+
+    def step_marked():
+        for L in layers:
+            for name, fn in layer_ops(ops, L, sh):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                marks.append((name, a, b))
+
+    graph_marked = capture(torch, step_marked, stream)
+    marks = marks[len(marks) // 2:]  # the events recorded during capture (second call)
+
+    sampler = ClockSampler(visible_index(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+
+    # ---- timed region: K graph replays of the step
+    for _ in range(args.warmup):
+        graph.replay()
+    barrier()
+    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+
+    # ---- per-kernel durations over K replays of the marked step
+    per_op = {n: [] for n in OPS}
+    reps = max(1, min(args.steps, 200))
+    for _ in range(reps):
+        graph_marked.replay()
+        torch.cuda.synchronize()
+        for name, a, b in marks:
+            per_op[name].append(a.elapsed_time(b))
+    if sampler:
+        sampler.stop()
+
+    # ---- e2e: pinned host inputs -> device, the step, results -> host
+    h2d_pairs, d2h_pairs = [], []
+    for L in layers:
+        for t in (L.mlp_out, L.res, L.q, L.k, L.attn_out, L.gate_up):
+            h2d_pairs.append((torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t), t))
+        for t in (L.res, L.h1, L.q, L.k, L.h2, L.act):
+            d2h_pairs.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
+    h2d_bytes = sum(d.numel() * d.element_size() for _, d in h2d_pairs)
+    d2h_bytes = sum(d.numel() * d.element_size() for d, _ in d2h_pairs)
+    e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        for h, d in h2d_pairs:
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        for d, h in d2h_pairs:
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        f1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1))
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    total_bytes = step_bytes * args.steps * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    e2e_value = step_bytes * e2e_steps * world / (e2e_ms * 1e-3) / 1e9
+
+    # dominant kernel: the largest share of the marked step's device time
+    op_ms = {n: float(np.sum(v)) for n, v in per_op.items()}
+    dom = max(op_ms, key=op_ms.get)
+    dom_launches = [x for x in per_op[dom]]
+    avg_us = float(np.mean(dom_launches)) * 1e3
+    achieved = OP_BYTES[dom] / (avg_us * 1e-6) / 1e9
+    kern = OP_KERNEL[dom]
+    roofline = {"bound": "hbm", "kernel": kern, "op": dom, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)",
+                "traffic": traffic_for(kern),
+                "bytes_per_launch": OP_BYTES[dom], "avg_launch_us": round(avg_us, 3),
+                "share": {n: round(op_ms[n] / sum(op_ms.values()), 4) for n in OPS}}
+
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else {}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode seams of a 36-layer decoder: per layer add_rmsnorm, "
+                               "qk_norm_rope, add_rmsnorm, silu_and_mul",
+                   "T": T_DEC, "hidden": HID, "gate": INTER, "heads": [HQ, HK], "head_dim": HD,
+                   "rotary": [HD, "rotate_half"], "layers": LAYERS, "global_batch": T_DEC * world,
+                   "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB per step, "
+                         "distinct buffers per layer",
+                   "graph": "one CUDA graph per step (144 launches)",
+                   "parallelism": f"replicas x{world}"},
+        "step_bytes": step_bytes,
+        "roofline": roofline,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps},
+        "clocks": clocks,
+    }
+    if world == 1:
+        line["t1_us_per_call"] = t1_latency(torch, ops, synth, device)
+        if not args.no_sweep:
+            line["sweep"] = sweep(torch, ops, synth, device, peak)
+            line["sweep_format"] = "T -> [us per call (cold L2), GB/s, fraction of peak]"
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

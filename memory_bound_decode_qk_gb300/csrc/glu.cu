@@ -1,0 +1,260 @@
+// glu.cu -- SiLU / tanh-GELU gated activations of a merged gate+up row (sm_103a).
+//
+// What it computes ("thox-edge-ops v2", section 5.1; FlashRT
+// gate_geglu_merged_fp8): out[t, i] = act(g) * u with g = gate_up[t, i],
+// u = gate_up[t, d + i].  The gate is the first half of each row.
+//   silu(g)      = g * sigma(g)
+//   gelu_tanh(g) = 0.5 g (1 + tanh z) = g * sigma(2z),
+//                  z = sqrt(2/pi) (g + 0.044715 g^3)
+// The second form is an exact identity, since 0.5 (1 + tanh z) equals the
+// logistic sigma(2z).  It avoids the cancellation of 1 + tanh z for negative
+// z.  sigma(v) is evaluated as num / (1 + e^-|v|) with num = 1 for v >= 0 and
+// e^-|v| otherwise, so nothing overflows.
+//
+// Two precisions of the exponential, both from this identity:
+//   - fp32 outputs: libm expf, an IEEE divide, and the GELU argument 2z
+//     carried as an unevaluated sum of two floats.  This keeps the relative
+//     error within a few fp32 ulps for every g.
+//   - bf16 / fp16 / FP8 outputs: e^-a = 2^(-a log2 e) through ex2.approx and
+//     a reciprocal through rcp.approx.  The error is a few fp32 ulps (plus
+//     the |2z| * 2^-24 of the argument's rounding), far inside half an ulp of
+//     the output in most cases.  This keeps the kernel HBM-bound rather than
+//     issue-bound at full bandwidth.
+//
+// GB300 design.  It is a pure stream: it reads 2 elements and writes 1 per
+// output.  The rows are flattened into one index space of 16-byte vectors.
+// Each thread issues its U gate and U up loads before any arithmetic.  A
+// multiply-high divide turns a flat index into (row, column).  Stores are
+// 16 bytes, or 8 bytes of E4M3 codes: four codes per 32-bit word.
+#include "edge_common.cuh"
+#include "fastdiv.h"
+#include "launch.h"
+
+namespace edge {
+namespace {
+
+constexpr int kSilu = 0;
+constexpr int kGelu = 1;
+
+// Constants from their definitions, split into a float and its remainder.
+constexpr double kLog2eD = 1.4426950408889634073599246810019;   // log2(e)
+constexpr double kK2D = 1.5957691216057307117597842397375;      // 2 sqrt(2/pi)
+constexpr double kCD = 0.044715;
+constexpr float kLog2e = (float)kLog2eD;
+constexpr float kK2 = (float)kK2D;
+constexpr float kK2lo = (float)(kK2D - (double)(float)kK2D);
+constexpr float kC = (float)kCD;
+constexpr float kClo = (float)(kCD - (double)(float)kCD);
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// act(g) * u, fast form (bf16 / fp16 / FP8 outputs).
+template <int ACT>
+__device__ __forceinline__ float gate_fast(float g, float u) {
+    float v;
+    if constexpr (ACT == kSilu) {
+        v = g;
+    } else {
+        const float c2 = __fmul_rn(__fmul_rn(kC, g), g);
+        v = __fmul_rn(__fmul_rn(kK2, g), __fadd_rn(1.0f, c2));
+    }
+    const float t = ex2_approx(__fmul_rn(-fabsf(v), kLog2e));
+    const float num = v >= 0.0f ? 1.0f : t;
+    return __fmul_rn(__fmul_rn(g, u), __fmul_rn(num, rcp_approx(__fadd_rn(1.0f, t))));
+}
+
+// act(g) * u, accurate form (fp32 outputs).
+template <int ACT>
+__device__ __forceinline__ float gate_accurate(float g, float u) {
+    float a, ae;  // |v| = a + ae, v the logistic argument
+    bool neg;
+    if constexpr (ACT == kSilu) {
+        a = fabsf(g);
+        ae = 0.0f;
+        neg = g < 0.0f;
+    } else {
+        // v = 2z = K g (1 + C g^2) in double-float arithmetic
+        const float g2 = __fmul_rn(g, g);
+        const float g2e = __fmaf_rn(g, g, -g2);
+        const float c = __fmul_rn(kC, g2);
+        const float ce = __fmaf_rn(kC, g2, -c) + __fmaf_rn(kC, g2e, __fmul_rn(kClo, g2));
+        const float s = __fadd_rn(1.0f, c);
+        const float bb = __fsub_rn(s, 1.0f);
+        const float se = __fadd_rn(__fadd_rn(__fsub_rn(1.0f, __fsub_rn(s, bb)), __fsub_rn(c, bb)), ce);
+        const float pq = __fmul_rn(g, s);
+        const float pe = __fmaf_rn(g, s, -pq) + __fmul_rn(g, se);
+        const float z = __fmul_rn(kK2, pq);
+        const float ze = __fmaf_rn(kK2, pq, -z) + __fmaf_rn(kK2, pe, __fmul_rn(kK2lo, pq));
+        neg = z < 0.0f;
+        a = fabsf(z);
+        ae = neg ? -ze : ze;
+    }
+    // e^-(a + ae) = e^-a * e^-ae ~= e^-a (1 - ae), |ae| <= a few ulp of a
+    const float t = __fmul_rn(expf(-a), __fsub_rn(1.0f, ae));
+    const float num = neg ? t : 1.0f;
+    return __fmul_rn(__fmul_rn(g, u), __fdiv_rn(num, __fadd_rn(1.0f, t)));
+}
+
+template <typename T, bool FP8, int ACT>
+__device__ __forceinline__ float gate(float g, float u) {
+    if constexpr (std::is_same<T, float>::value && !FP8) {
+        return gate_accurate<ACT>(g, u);
+    } else {
+        return gate_fast<ACT>(g, u);
+    }
+}
+
+struct GluP {
+    const char* gu;
+    char* out;
+    uint32_t total;   // rows * dvec (vector path) or rows * d (generic, 64-bit below)
+    FastDiv dv;       // 16-byte vectors per half row
+    int64_t rows;
+    int64_t d;
+    float inv;
+};
+
+template <typename T, bool FP8, int ACT, int U>
+__global__ void __launch_bounds__(256) glu_vec_kernel(GluP p) {
+    constexpr int N = vec_elems<T>();
+    const uint32_t dv = p.dv.d;
+    const uint4* gu = reinterpret_cast<const uint4*>(p.gu);
+    const uint32_t stride = gridDim.x * blockDim.x * U;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (uint32_t b0 = blockIdx.x * blockDim.x * U + threadIdx.x; b0 < p.total; b0 += stride) {
+        uint4 gv[U], uv[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const uint32_t i = b0 + k * blockDim.x;
+            if (i < p.total) {
+                const uint32_t row = fast_div(i, p.dv);
+                const uint32_t col = i - row * dv;
+                const uint4* g = gu + (size_t)row * 2 * dv + col;
+                gv[k] = __ldcs(g);
+                uv[k] = __ldcs(g + dv);
+            } else {
+                gv[k] = make_uint4(0u, 0u, 0u, 0u);
+                uv[k] = gv[k];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const uint32_t i = b0 + k * blockDim.x;
+            if (i >= p.total) continue;
+            float g[N], u[N], y[N];
+            unpack_vec<T, N>(gv[k], g);
+            unpack_vec<T, N>(uv[k], u);
+#pragma unroll
+            for (int e = 0; e < N; ++e) y[e] = gate<T, FP8, ACT>(g[e], u[e]);
+            if constexpr (FP8) {
+                auto q8 = quantize_vec<N>(y, p.inv);
+                reinterpret_cast<decltype(q8)*>(p.out)[i] = q8;
+            } else {
+                reinterpret_cast<uint4*>(p.out)[i] = pack_vec<T, N>(y);
+            }
+        }
+    }
+}
+
+template <typename T, bool FP8, int ACT>
+__global__ void __launch_bounds__(256) glu_generic_kernel(GluP p) {
+    const T* gu = reinterpret_cast<const T*>(p.gu);
+    const int64_t total = p.rows * p.d;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t row = i / p.d;
+        const int64_t col = i - row * p.d;
+        const float g = to_f(gu[row * 2 * p.d + col]);
+        const float u = to_f(gu[row * 2 * p.d + p.d + col]);
+        const float y = gate<T, FP8, ACT>(g, u);
+        if constexpr (FP8) {
+            reinterpret_cast<uint8_t*>(p.out)[i] = quantize1(y, p.inv);
+        } else {
+            reinterpret_cast<T*>(p.out)[i] = from_f<T>(y);
+        }
+    }
+}
+
+template <typename T, bool FP8, int ACT>
+cudaError_t launch_typed(const GluArgs& a, GluP& p, cudaStream_t s) {
+    constexpr int N = vec_elems<T>();
+    auto aligned = [](const void* ptr, uintptr_t n) {
+        return (reinterpret_cast<uintptr_t>(ptr) % n) == 0;
+    };
+    const int sms = sm_count();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+
+    const int64_t dvec = a.d / N;
+    const bool vec = (a.d * (int64_t)sizeof(T)) % 16 == 0 && aligned(a.gate_up, 16) &&
+                     aligned(a.out, FP8 ? N : 16) && a.rows * dvec <= kMaxUnits;
+    if (vec) {
+        constexpr int U = 2;
+        p.dv = make_fastdiv((uint32_t)dvec);
+        p.total = (uint32_t)(a.rows * dvec);
+        const int threads = 256;
+        int64_t blocks = ((int64_t)p.total + threads * U - 1) / (threads * U);
+        const int64_t cap = (int64_t)sms * (2048 / threads) * 16;
+        if (blocks > cap) blocks = cap;
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(threads);
+        return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, U>, p);
+    }
+    const int64_t total = a.rows * a.d;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)sms * 64;
+    if (blocks > cap) blocks = cap;
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&cfg, glu_generic_kernel<T, FP8, ACT>, p);
+}
+
+template <typename T>
+cudaError_t launch_dt(const GluArgs& a, GluP& p, cudaStream_t s) {
+    const bool fp8 = a.out_dt == kFP8;
+    if (a.act == kSilu) {
+        return fp8 ? launch_typed<T, true, kSilu>(a, p, s) : launch_typed<T, false, kSilu>(a, p, s);
+    }
+    return fp8 ? launch_typed<T, true, kGelu>(a, p, s) : launch_typed<T, false, kGelu>(a, p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_glu(const GluArgs& a, cudaStream_t s) {
+    GluP p;
+    p.gu = static_cast<const char*>(a.gate_up);
+    p.out = static_cast<char*>(a.out);
+    p.total = 0;
+    p.dv = make_fastdiv(1);
+    p.rows = a.rows;
+    p.d = a.d;
+    p.inv = a.inv_scale;
+    switch (a.dt) {
+        case kF32: return launch_dt<float>(a, p, s);
+        case kF16: return launch_dt<__half>(a, p, s);
+        default: return launch_dt<__nv_bfloat16>(a, p, s);
+    }
+}
+
+}  // namespace edge

@@ -1,0 +1,393 @@
+// qk_norm_rope.cu -- fused per-head QK-RMSNorm + RoPE prologue (sm_103a).
+//
+// What it computes ("thox-edge-ops v2", sections 5.1 and 5.4; ninfer text
+// profile, "Implementation"): every head of q (weight wq) and of k (weight wk)
+// of token t is normalized by its own RMSNorm and rounded to the activation
+// dtype.  If 0 <= positions[t] < cache_len, the first rotary_dim channels are
+// then rotated by cos/sin row positions[t] and rounded once more.  Channels
+// past rotary_dim carry the rounded normalized value.  An out-of-cache token
+// is normalized, not rotated, and reads no cache row.
+//
+// GB300 design.  The op is HBM-bound: it reads each head once and writes it
+// once, about 2 flops per byte.  One head is a "unit".  Fast path: a head of
+// D elements is held by LPH = D*s/16 lanes, one 16-byte vector per lane, so a
+// warp holds 32/LPH heads (bf16 D=256: one head per warp; bf16 D=128: two).
+//   - The sum of squares is reduced with xor-shuffles inside the lane group.
+//   - The rotate-half partner vector sits half/N lanes away and comes over a
+//     shuffle.  Interleaved pairs sit inside one vector.
+//   - cos/sin entries are read from L1: every head of a token shares the row.
+// Units are ordered token-major, so the warps of a CTA share cos/sin rows and
+// the norm weights.  Streamed inputs use evict-first loads.
+// Generic path: one warp per head, staged through shared memory.  It serves
+// any head_dim up to 2048, any even rotary_dim and any element-aligned
+// pointer.
+#include "edge_common.cuh"
+#include "fastdiv.h"
+#include "launch.h"
+
+namespace edge {
+namespace {
+
+constexpr int kRotateHalf = 0;
+constexpr int kInterleaved = 1;
+
+struct QKP {
+    const char* q;
+    const char* k;
+    char* qo;
+    char* ko;
+    const char* wq;
+    const char* wk;
+    const int64_t* pos;
+    const float* cs;
+    const float* sn;
+    int64_t cache_len;
+    uint32_t units;        // tokens * (q_heads + k_heads)
+    FastDiv heads;         // q_heads + k_heads
+    int q_heads, k_heads, D, rot, half;
+    int in_bytes, out_bytes;  // element sizes of input and output
+    float eps, delta, inv, fD;
+};
+
+struct Unit {
+    const char* src;
+    char* dst;
+    const char* w;
+    int64_t t;
+};
+
+__device__ __forceinline__ Unit locate(const QKP& p, uint32_t u) {
+    uint32_t t = fast_div(u, p.heads);
+    int h = (int)(u - t * p.heads.d);
+    Unit r;
+    r.t = t;
+    int64_t row;
+    if (h < p.q_heads) {
+        row = (int64_t)t * p.q_heads + h;
+        r.src = p.q + row * p.D * p.in_bytes;
+        r.dst = p.qo + row * p.D * p.out_bytes;
+        r.w = p.wq;
+    } else {
+        row = (int64_t)t * p.k_heads + (h - p.q_heads);
+        r.src = p.k + row * p.D * p.in_bytes;
+        r.dst = p.ko + row * p.D * p.out_bytes;
+        r.w = p.wk;
+    }
+    return r;
+}
+
+// ---------------------------------------------------------------- fast path
+
+template <typename T, bool FP8, int LPH, int LAYOUT>
+__global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
+    constexpr int N = vec_elems<T>();
+    constexpr int HPW = 32 / LPH;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (LPH - 1);
+    const int slot = lane / LPH;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (uint32_t base = warp * HPW; base < p.units; base += nwarps * HPW) {
+        const uint32_t u = base + slot;
+        const bool active = u < p.units;
+        Unit un = locate(p, active ? u : base);
+
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        int64_t pos = -1;
+        if (active) {
+            raw = __ldcs(reinterpret_cast<const uint4*>(un.src) + sub);
+            if (p.rot > 0) pos = __ldg(p.pos + un.t);
+        }
+        float w[N];
+        if (un.w != nullptr) {
+            uint4 wr = __ldg(reinterpret_cast<const uint4*>(un.w) + sub);
+            unpack_vec<T, N>(wr, w);
+#pragma unroll
+            for (int i = 0; i < N; ++i) w[i] = __fadd_rn(w[i], p.delta);
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) w[i] = 1.0f;
+        }
+
+        float x[N];
+        unpack_vec<T, N>(raw, x);
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+        ss = group_sum<LPH>(ss);
+        const float r = inv_rms(ss, p.fD, p.eps);
+
+        // normalized value, rounded to the activation dtype before the rotation
+        float m[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) m[i] = round_to<T>(__fmul_rn(__fmul_rn(x[i], r), w[i]));
+
+        const bool rot = active && pos >= 0 && pos < p.cache_len;
+        const int e0 = sub * N;  // first channel held by this lane
+        float y[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) y[i] = m[i];
+
+        if constexpr (LAYOUT == kInterleaved) {
+            if (rot && e0 < p.rot) {
+                // pairs (e0 + 2i, e0 + 2i + 1) use cache entries e0/2 + i
+                const float* crow = p.cs + pos * p.half + e0 / 2;
+                const float* srow = p.sn + pos * p.half + e0 / 2;
+                float c[N / 2], s[N / 2];
+                if constexpr (N == 8) {
+                    float4 c4 = __ldg(reinterpret_cast<const float4*>(crow));
+                    float4 s4 = __ldg(reinterpret_cast<const float4*>(srow));
+                    c[0] = c4.x; c[1] = c4.y; c[2] = c4.z; c[3] = c4.w;
+                    s[0] = s4.x; s[1] = s4.y; s[2] = s4.z; s[3] = s4.w;
+                } else {
+                    float2 c2 = __ldg(reinterpret_cast<const float2*>(crow));
+                    float2 s2 = __ldg(reinterpret_cast<const float2*>(srow));
+                    c[0] = c2.x; c[1] = c2.y;
+                    s[0] = s2.x; s[1] = s2.y;
+                }
+#pragma unroll
+                for (int i = 0; i < N / 2; ++i) {
+                    const float a = m[2 * i], b = m[2 * i + 1];
+                    y[2 * i] = __fmaf_rn(a, c[i], -__fmul_rn(b, s[i]));
+                    y[2 * i + 1] = __fmaf_rn(b, c[i], __fmul_rn(a, s[i]));
+                }
+            }
+        } else {
+            // rotate-half: channel e pairs with e + half; the partner vector is
+            // held by the lane half/N positions away in the same head group
+            const int hv = p.half / N;
+            int role = 0;  // 1: first member (a), 2: second member (b)
+            if (rot) role = e0 < p.half ? 1 : (e0 < p.rot ? 2 : 0);
+            const int src = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
+            const uint4 mine = pack_vec<T, N>(m);  // exact: m is already rounded to T
+            uint4 other;
+            other.x = __shfl_sync(0xffffffffu, mine.x, src);
+            other.y = __shfl_sync(0xffffffffu, mine.y, src);
+            other.z = __shfl_sync(0xffffffffu, mine.z, src);
+            other.w = __shfl_sync(0xffffffffu, mine.w, src);
+            if (role != 0) {
+                float pm[N];
+                unpack_vec<T, N>(other, pm);
+                const int j0 = role == 1 ? e0 : e0 - p.half;
+                const float4* c4 = reinterpret_cast<const float4*>(p.cs + pos * p.half + j0);
+                const float4* s4 = reinterpret_cast<const float4*>(p.sn + pos * p.half + j0);
+                float c[N], s[N];
+#pragma unroll
+                for (int v = 0; v < N / 4; ++v) {
+                    float4 cc = __ldg(c4 + v), sv = __ldg(s4 + v);
+                    c[4 * v] = cc.x; c[4 * v + 1] = cc.y; c[4 * v + 2] = cc.z; c[4 * v + 3] = cc.w;
+                    s[4 * v] = sv.x; s[4 * v + 1] = sv.y; s[4 * v + 2] = sv.z; s[4 * v + 3] = sv.w;
+                }
+                if (role == 1) {
+#pragma unroll
+                    for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(m[i], c[i], -__fmul_rn(pm[i], s[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(m[i], c[i], __fmul_rn(pm[i], s[i]));
+                }
+            }
+        }
+
+        if (active) {
+            if constexpr (FP8) {
+                auto q8 = quantize_vec<N>(y, p.inv);
+                reinterpret_cast<decltype(q8)*>(un.dst)[sub] = q8;
+            } else {
+                reinterpret_cast<uint4*>(un.dst)[sub] = pack_vec<T, N>(y);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- generic path
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const char* base, int i) {
+    return to_f(reinterpret_cast<const T*>(base)[i]);
+}
+
+template <typename T, bool FP8>
+__global__ void __launch_bounds__(128) qk_generic_kernel(QKP p, int layout) {
+    extern __shared__ float smem[];
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    float* hm = smem + wib * p.D;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (uint32_t u = warp; u < p.units; u += nwarps) {
+        Unit un = locate(p, u);
+        float ss = 0.0f;
+        for (int e = lane; e < p.D; e += 32) {
+            float v = ld_elem<T>(un.src, e);
+            hm[e] = v;
+            ss = __fmaf_rn(v, v, ss);
+        }
+        ss = group_sum<32>(ss);
+        const float r = inv_rms(ss, p.fD, p.eps);
+        for (int e = lane; e < p.D; e += 32) {
+            float w = un.w ? __fadd_rn(ld_elem<T>(un.w, e), p.delta) : 1.0f;
+            hm[e] = round_to<T>(__fmul_rn(__fmul_rn(hm[e], r), w));
+        }
+        __syncwarp();
+        int64_t pos = -1;
+        if (p.rot > 0) pos = p.pos[un.t];
+        const bool rot = pos >= 0 && pos < p.cache_len;
+        for (int e = lane; e < p.D; e += 32) {
+            float y = hm[e];
+            if (rot && e < p.rot) {
+                int j, partner;
+                bool first;
+                if (layout == kInterleaved) {
+                    j = e >> 1;
+                    partner = e ^ 1;
+                    first = (e & 1) == 0;
+                } else {
+                    first = e < p.half;
+                    j = first ? e : e - p.half;
+                    partner = first ? e + p.half : e - p.half;
+                }
+                const float c = p.cs[pos * p.half + j];
+                const float sn = p.sn[pos * p.half + j];
+                const float other = hm[partner];
+                y = first ? __fmaf_rn(y, c, -__fmul_rn(other, sn))
+                          : __fmaf_rn(y, c, __fmul_rn(other, sn));
+            }
+            if constexpr (FP8) {
+                reinterpret_cast<uint8_t*>(un.dst)[e] = quantize1(y, p.inv);
+            } else {
+                reinterpret_cast<T*>(un.dst)[e] = from_f<T>(y);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------- launch
+
+template <typename T, bool FP8>
+cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
+    constexpr int N = vec_elems<T>();
+    const int D = a.head_dim;
+    const int nvec = (D * (int)sizeof(T)) % 16 == 0 ? D * (int)sizeof(T) / 16 : 0;
+    auto aligned = [](const void* ptr, uintptr_t n) {
+        return ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) % n) == 0;
+    };
+    bool vec = nvec > 0 && nvec <= 32 && (nvec & (nvec - 1)) == 0;
+    vec = vec && aligned(a.q, 16) && aligned(a.k, 16) && aligned(a.wq, 16) && aligned(a.wk, 16);
+    vec = vec && aligned(a.q_out, FP8 ? N : 16) && aligned(a.k_out, FP8 ? N : 16);
+    if (a.rotary_dim > 0) {
+        if (a.layout == kInterleaved) {
+            vec = vec && a.rotary_dim % N == 0 && aligned(a.cos, 8 * (N / 4)) &&
+                  aligned(a.sin, 8 * (N / 4));
+        } else {
+            vec = vec && (a.rotary_dim / 2) % N == 0 && aligned(a.cos, 16) && aligned(a.sin, 16);
+        }
+    }
+    const int sms = sm_count();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+
+    if (vec) {
+        const int lph = nvec;
+        const int hpw = 32 / lph;
+        const int threads = 256;
+        const int64_t per_block = (int64_t)(threads / 32) * hpw;
+        int64_t blocks = ((int64_t)p.units + per_block - 1) / per_block;
+        const int64_t cap = (int64_t)sms * (2048 / threads) * 8;
+        if (blocks > cap) blocks = cap;
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = 0;
+#define EDGE_QK_CASE(L)                                                                 \
+    case L:                                                                              \
+        return a.layout == kInterleaved                                                 \
+                   ? cudaLaunchKernelEx(&cfg, qk_vec_kernel<T, FP8, L, kInterleaved>, p) \
+                   : cudaLaunchKernelEx(&cfg, qk_vec_kernel<T, FP8, L, kRotateHalf>, p);
+        switch (lph) {
+            EDGE_QK_CASE(1)
+            EDGE_QK_CASE(2)
+            EDGE_QK_CASE(4)
+            EDGE_QK_CASE(8)
+            EDGE_QK_CASE(16)
+            EDGE_QK_CASE(32)
+            default:
+                break;
+        }
+#undef EDGE_QK_CASE
+    }
+    const int threads = 128;
+    const int64_t warps_per_block = threads / 32;
+    int64_t blocks = ((int64_t)p.units + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = (int64_t)sms * 16;
+    if (blocks > cap) blocks = cap;
+    const size_t smem = (size_t)warps_per_block * D * sizeof(float);
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(qk_generic_kernel<T, FP8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaLaunchKernelEx(&cfg, qk_generic_kernel<T, FP8>, p, a.layout);
+}
+
+}  // namespace
+
+cudaError_t launch_qk(const QKArgs& args, cudaStream_t s) {
+    // With no cache rows or no positions no token can rotate: run the
+    // prologue with rotary width 0 so the kernels touch neither pointer.
+    QKArgs a = args;
+    if (a.cache_len <= 0 || a.pos == nullptr || a.cos == nullptr || a.sin == nullptr) {
+        a.rotary_dim = 0;
+    }
+    QKP p;
+    p.q = static_cast<const char*>(a.q);
+    p.k = static_cast<const char*>(a.k);
+    p.qo = static_cast<char*>(a.q_out);
+    p.ko = static_cast<char*>(a.k_out);
+    p.wq = static_cast<const char*>(a.wq);
+    p.wk = static_cast<const char*>(a.wk);
+    p.pos = a.pos;
+    p.cs = a.cos;
+    p.sn = a.sin;
+    p.cache_len = a.rotary_dim > 0 ? a.cache_len : 0;
+    p.units = (uint32_t)(a.tokens * (a.q_heads + a.k_heads));
+    p.heads = make_fastdiv((uint32_t)(a.q_heads + a.k_heads));
+    p.q_heads = a.q_heads;
+    p.k_heads = a.k_heads;
+    p.D = a.head_dim;
+    p.rot = a.rotary_dim;
+    p.half = a.rotary_dim / 2;
+    p.in_bytes = a.dt == kF32 ? 4 : 2;
+    p.out_bytes = a.out_dt == kFP8 ? 1 : p.in_bytes;
+    p.eps = a.eps;
+    p.delta = (float)a.weight_offset;
+    p.inv = a.inv_scale;
+    p.fD = (float)a.head_dim;
+    const bool fp8 = a.out_dt == kFP8;
+    switch (a.dt) {
+        case kF32:
+            return fp8 ? launch_typed<float, true>(a, p, s) : launch_typed<float, false>(a, p, s);
+        case kF16:
+            return fp8 ? launch_typed<__half, true>(a, p, s) : launch_typed<__half, false>(a, p, s);
+        default:
+            return fp8 ? launch_typed<__nv_bfloat16, true>(a, p, s)
+                       : launch_typed<__nv_bfloat16, false>(a, p, s);
+    }
+}
+
+}  // namespace edge

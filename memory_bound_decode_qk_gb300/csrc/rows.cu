@@ -1,0 +1,255 @@
+// rows.cu -- RMSNorm and fused residual-add RMSNorm over rows (sm_103a).
+//
+// What they compute ("thox-edge-ops v2", section 3 R1 and section 5.1;
+// FlashRT rms_norm_fp8_static, residual_add_rms_norm_fp8_static and the
+// no-weight RMSNorm):
+//   residual <- round_dt(fp32(x) + fp32(residual))    (fused form only)
+//   out      =  s * r * (w + delta),  r = 1 / sqrt(mean(s^2) + eps)
+// s is x for the plain form and the rounded sum for the fused form.  The
+// output is rounded once to the activation dtype, or takes the static-scale
+// FP8 epilogue.
+//
+// GB300 design.  Both ops move about 3 or 4 bytes of HBM traffic for every 2
+// flops.  A row is held in registers from its load to its store, so it makes
+// one HBM pass.  W warps own a row.  Each thread holds up to V 16-byte
+// vectors, and all of its loads are issued before any arithmetic, so a thread
+// keeps V (fused form: 2V) loads in flight.  The sum of squares is reduced
+// with warp shuffles, and through shared memory when W > 1.  W and V come
+// from the row length and the row count: few rows spread over more warps,
+// many rows favour more bytes in flight per thread.  Rows whose length or
+// alignment does not allow 16-byte vectors take a scalar two-pass kernel:
+// one CTA per row, and the second pass re-reads the row from L1/L2.
+#include "edge_common.cuh"
+#include "launch.h"
+
+namespace edge {
+namespace {
+
+struct RowsP {
+    const char* x;
+    char* res;
+    const char* w;
+    char* out;
+    int64_t rows;
+    int hidden;
+    int nvec;      // 16-byte vectors per row
+    int W;         // warps per row
+    int RPB;       // rows per CTA
+    float eps, delta, inv, fH;
+};
+
+template <typename T, bool FP8, bool ADD, int V>
+__global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
+    constexpr int N = vec_elems<T>();
+    __shared__ float red[16];
+    const int tpr = 32 * p.W;
+    const int g = threadIdx.x / tpr;
+    const int tid = threadIdx.x - g * tpr;
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int64_t in_row = (int64_t)p.hidden * (int64_t)sizeof(T);
+    const int64_t out_row = FP8 ? (int64_t)p.hidden : in_row;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (int64_t r0 = (int64_t)blockIdx.x * p.RPB; r0 < p.rows; r0 += (int64_t)gridDim.x * p.RPB) {
+        const int64_t row = r0 + g;
+        const bool active = row < p.rows;
+        const int64_t rsafe = active ? row : r0;
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + rsafe * in_row);
+        uint4* rr = ADD ? reinterpret_cast<uint4*>(p.res + rsafe * in_row) : nullptr;
+
+        uint4 xv[V], rv[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int idx = tid + i * tpr;
+            const bool ok = active && idx < p.nvec;
+            xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (ADD) rv[i] = ok ? __ldcs(rr + idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
+
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float a[N];
+            unpack_vec<T, N>(xv[i], a);
+            if constexpr (ADD) {
+                // eager semantics: widen, add in fp32, round once to the dtype
+                float b[N];
+                unpack_vec<T, N>(rv[i], b);
+#pragma unroll
+                for (int e = 0; e < N; ++e) a[e] = round_to<T>(__fadd_rn(a[e], b[e]));
+                xv[i] = pack_vec<T, N>(a);
+                const int idx = tid + i * tpr;
+                if (active && idx < p.nvec) rr[idx] = xv[i];
+            }
+#pragma unroll
+            for (int e = 0; e < N; ++e) ss = __fmaf_rn(a[e], a[e], ss);
+        }
+        ss = group_sum<32>(ss);
+        if (p.W > 1) {
+            if (lane == 0) red[wib] = ss;
+            __syncthreads();
+            ss = 0.0f;
+            for (int k = 0; k < p.W; ++k) ss = __fadd_rn(ss, red[g * p.W + k]);
+            __syncthreads();
+        }
+        const float r = inv_rms(ss, p.fH, p.eps);
+
+        const uint4* wv = reinterpret_cast<const uint4*>(p.w);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int idx = tid + i * tpr;
+            if (!(active && idx < p.nvec)) continue;
+            float s[N], y[N];
+            unpack_vec<T, N>(xv[i], s);
+            if (wv != nullptr) {
+                float w[N];
+                unpack_vec<T, N>(__ldg(wv + idx), w);
+#pragma unroll
+                for (int e = 0; e < N; ++e) y[e] = __fmul_rn(__fmul_rn(s[e], r), __fadd_rn(w[e], p.delta));
+            } else {
+#pragma unroll
+                for (int e = 0; e < N; ++e) y[e] = __fmul_rn(s[e], r);
+            }
+            char* orow = p.out + row * out_row;
+            if constexpr (FP8) {
+                auto q8 = quantize_vec<N>(y, p.inv);
+                reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
+            } else {
+                reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
+            }
+        }
+    }
+}
+
+template <typename T, bool FP8, bool ADD>
+__global__ void __launch_bounds__(256) rows_generic_kernel(RowsP p) {
+    __shared__ float red[8];
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const T* x = reinterpret_cast<const T*>(p.x) + row * p.hidden;
+        T* res = ADD ? reinterpret_cast<T*>(p.res) + row * p.hidden : nullptr;
+        float ss = 0.0f;
+        for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
+            float a = to_f(x[i]);
+            if constexpr (ADD) {
+                a = round_to<T>(__fadd_rn(a, to_f(res[i])));
+                res[i] = from_f<T>(a);
+            }
+            ss = __fmaf_rn(a, a, ss);
+        }
+        ss = group_sum<32>(ss);
+        if (lane == 0) red[wib] = ss;
+        __syncthreads();
+        ss = 0.0f;
+        for (int k = 0; k < nw; ++k) ss = __fadd_rn(ss, red[k]);
+        __syncthreads();
+        const float r = inv_rms(ss, p.fH, p.eps);
+        const T* w = reinterpret_cast<const T*>(p.w);
+        for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
+            const float s = ADD ? to_f(res[i]) : to_f(x[i]);
+            const float y = w ? __fmul_rn(__fmul_rn(s, r), __fadd_rn(to_f(w[i]), p.delta))
+                              : __fmul_rn(s, r);
+            if constexpr (FP8) {
+                reinterpret_cast<uint8_t*>(p.out)[row * p.hidden + i] = quantize1(y, p.inv);
+            } else {
+                reinterpret_cast<T*>(p.out)[row * p.hidden + i] = from_f<T>(y);
+            }
+        }
+    }
+}
+
+template <typename T, bool FP8, bool ADD>
+cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
+    constexpr int N = vec_elems<T>();
+    auto aligned = [](const void* ptr, uintptr_t n) {
+        return ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) % n) == 0;
+    };
+    const int sms = sm_count();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+
+    const bool vec_ok = (a.hidden * (int64_t)sizeof(T)) % 16 == 0 && aligned(a.x, 16) &&
+                        aligned(a.residual, 16) && aligned(a.w, 16) &&
+                        aligned(a.out, FP8 ? N : 16);
+    const int64_t nvec = a.hidden / N;
+    if (vec_ok && nvec <= 16 * 32 * 8) {
+        // vectors per thread: many rows -> more bytes in flight per thread;
+        // few rows -> spread each row over more warps
+        const int vt = a.rows >= 2 * sms ? 4 : 2;
+        int W = (int)((nvec + 32 * vt - 1) / (32 * vt));
+        if (W > 16) W = 16;
+        const int64_t per = (nvec + 32 * W - 1) / (32 * W);
+        int V = per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
+        int RPB = 256 / (32 * W);
+        if (RPB < 1) RPB = 1;
+        p.nvec = (int)nvec;
+        p.W = W;
+        p.RPB = RPB;
+        const int threads = 32 * W * RPB;
+        int64_t blocks = (a.rows + RPB - 1) / RPB;
+        const int64_t cap = (int64_t)sms * (2048 / threads) * 8;
+        if (blocks > cap) blocks = cap;
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(threads);
+        switch (V) {
+            case 1: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 1>, p);
+            case 2: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 2>, p);
+            case 4: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 4>, p);
+            default: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 8>, p);
+        }
+    }
+    int64_t blocks = a.rows;
+    const int64_t cap = (int64_t)sms * 16;
+    if (blocks > cap) blocks = cap;
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&cfg, rows_generic_kernel<T, FP8, ADD>, p);
+}
+
+template <typename T>
+cudaError_t launch_dt(const RowsArgs& a, RowsP& p, cudaStream_t s) {
+    const bool fp8 = a.out_dt == kFP8;
+    const bool add = a.residual != nullptr;
+    if (fp8) return add ? launch_typed<T, true, true>(a, p, s) : launch_typed<T, true, false>(a, p, s);
+    return add ? launch_typed<T, false, true>(a, p, s) : launch_typed<T, false, false>(a, p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s) {
+    RowsP p;
+    p.x = static_cast<const char*>(a.x);
+    p.res = static_cast<char*>(a.residual);
+    p.w = static_cast<const char*>(a.w);
+    p.out = static_cast<char*>(a.out);
+    p.rows = a.rows;
+    p.hidden = (int)a.hidden;
+    p.nvec = 0;
+    p.W = 1;
+    p.RPB = 1;
+    p.eps = a.eps;
+    p.delta = (float)a.weight_offset;
+    p.inv = a.inv_scale;
+    p.fH = (float)a.hidden;
+    switch (a.dt) {
+        case kF32: return launch_dt<float>(a, p, s);
+        case kF16: return launch_dt<__half>(a, p, s);
+        default: return launch_dt<__nv_bfloat16>(a, p, s);
+    }
+}
+
+}  // namespace edge

@@ -55,6 +55,26 @@ def ulp_distance(a: np.ndarray, b: np.ndarray, fmt: int) -> np.ndarray:
     return np.abs(ordered(a, fmt) - ordered(b, fmt))
 
 
+_MANT = {oracle.F16: 10, oracle.BF16: 7, oracle.E4M3: 3, oracle.F32: 23}
+_EMIN = {oracle.F16: -14, oracle.BF16: -126, oracle.E4M3: -6, oracle.F32: -126}
+
+
+def ulp_at(x: np.ndarray, fmt: int) -> np.ndarray:
+    """Spacing of format ``fmt`` at magnitude x (the subnormal spacing below the normals)."""
+    x = np.abs(np.asarray(x, np.float64))
+    e = np.where(x > 0, np.floor(np.log2(np.where(x > 0, x, 1.0))), _EMIN[fmt])
+    e = np.maximum(e, _EMIN[fmt])
+    return np.ldexp(1.0, (e - _MANT[fmt]).astype(np.int64))
+
+
+def within_one_ulp(got: np.ndarray, ref: np.ndarray, mag: np.ndarray, fmt: int) -> np.ndarray:
+    """|got - ref| <= one ulp of the format at max(|ref|, mag).  For a rotated
+    channel mag is the pair norm, which absorbs the cancellation of a c - b s."""
+    g = oracle.decode(got, fmt)
+    r = oracle.decode(ref, fmt)
+    return np.abs(g - r) <= ulp_at(np.maximum(np.abs(r), mag), fmt)
+
+
 def _round_codes(v: np.ndarray, out_fmt: int, inv_scale: float) -> np.ndarray:
     if out_fmt == oracle.E4M3:
         return oracle.quantize(v, inv_scale)

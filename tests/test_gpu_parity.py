@@ -1,0 +1,470 @@
+"""GPU parity: every op through the C ABI against the CPU oracle.
+
+The inputs are seeded and shaped like the five workloads.  The sizes span
+several tiles and a ragged tail, and edge cases are included.  Bars:
+  * the residual sum is bit-exact;
+  * bf16/fp16 outputs are within 1 ulp, and pass the strict check (bit-exact
+    except within a derived band eta around rounding midpoints);
+  * FP8 codes are bit-exact outside that band;
+  * fp32 outputs are within a relative error of 2e-6 of the exact value (at
+    the pair norm for rotated channels).
+Every output sits between guard regions that must come back untouched.
+
+Bands, from the kernels' fp32 arithmetic (u = 2^-24):
+  ETA_NORM = 2^-18 (64u).  This covers the sum of squares over a thread's
+    sequential elements plus the shuffle tree (under 40u, since every term is
+    positive), the correctly rounded divide, square root and reciprocal, and
+    the three products.
+  gates:   (10 + 2|g|) u for SiLU and (10 + 5|2z|) u for tanh-GELU.  Both
+    come from the exponential of a rounded argument through ex2.approx and
+    rcp.approx.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import TORCH_FMT, f32_ok, report, storage, strict_ok, ulp_distance, within_one_ulp
+from memory_bound_decode_qk_gb300 import edge_ops, synth
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -24
+ETA_NORM = 2.0 ** -18
+GUARD = 256  # bytes on each side of every output
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    edge_ops.lib(build_if_missing=True)
+
+
+# ---------------------------------------------------------------- plumbing
+
+class Guarded:
+    """An output tensor between guard bytes filled with a known pattern."""
+
+    def __init__(self, shape, dtype, misalign_elems=0):
+        esz = torch.empty((), dtype=dtype).element_size()
+        n = int(np.prod(shape))
+        self.off = GUARD + misalign_elems * esz
+        self.nbytes = n * esz
+        self.raw = torch.empty(self.off + self.nbytes + GUARD, dtype=torch.uint8, device="cuda")
+        self.raw.fill_(0xA5)
+        self.t = self.raw[self.off:self.off + self.nbytes].view(dtype).view(shape)
+
+    def check(self):
+        r = self.raw.cpu().numpy()
+        assert np.all(r[:self.off] == 0xA5), "write before the output"
+        assert np.all(r[self.off + self.nbytes:] == 0xA5), "write past the output"
+
+
+def dev(t, misalign_elems=0):
+    """Copy a CPU tensor to the device, optionally at an element-misaligned address."""
+    if t is None:
+        return None
+    if not misalign_elems:
+        return t.contiguous().cuda()
+    flat = torch.empty(t.numel() + misalign_elems, dtype=t.dtype, device="cuda")
+    v = flat[misalign_elems:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def calib_inv(pre):
+    """Static calibration: scale = amax / 448 of a calibration pass, inv = 1 / scale (fp32)."""
+    amax = float(np.abs(pre).max())
+    return float(np.float32(1.0) / np.float32(amax / 448.0))
+
+
+def check_dtype_out(name, got, ref_bits, pre, mag, fmt, eta, alt=None):
+    """bf16/fp16: <= 1 ulp everywhere (at the pair norm for rotated channels)
+    and the strict check."""
+    one = within_one_ulp(got, ref_bits, mag, fmt)
+    assert one.all(), report(name + " (1 ulp)", one)
+    d = ulp_distance(got, ref_bits, fmt)
+    ok = strict_ok(got, pre, mag, fmt, eta, alt=alt)
+    assert ok.all(), report(name, ok)
+    return float(np.mean(d == 0))
+
+
+def check_fp8_out(name, got, pre, mag, eta, inv, alt=None):
+    ok = strict_ok(got, pre, mag, oracle.E4M3, eta, inv_scale=inv, alt=alt)
+    assert ok.all(), report(name, ok)
+
+
+def check_out(name, got, ref_bits, pre, mag, fmt, out_fmt, eta, inv=1.0, alt=None):
+    if out_fmt == oracle.E4M3:
+        check_fp8_out(name, got, pre, mag, eta, inv, alt)
+    elif fmt == oracle.F32:
+        ok = f32_ok(got, pre, mag, 2e-6)
+        assert ok.all(), report(name, ok)
+    else:
+        check_dtype_out(name, got, ref_bits, pre, mag, fmt, eta, alt)
+
+
+# ---------------------------------------------------------------- QK prologue
+
+QK_CASES = {
+    # workload 1: fp32, D=128 full rotate-half, (8,2), T=4, one token out of cache, in place
+    "cfg1_f32": dict(dtype=torch.float32, T=4, Hq=8, Hk=2, D=128, rot=128, layout=0,
+                     w_mean=0.0, w_std=0.1, offset=1, theta=1e6, P=4096,
+                     positions="cfg_out_of_cache", inplace=True),
+    # workload 3: text profile, bf16 out of place, partial rotary 64 of 256
+    "cfg3_16_2_T1": dict(dtype=torch.bfloat16, T=1, Hq=16, Hk=2, D=256, rot=64, layout=0,
+                         w_mean=0.0, w_std=0.05, offset=1, theta=1e7, P=32768, positions="offset"),
+    "cfg3_24_4_T8": dict(dtype=torch.bfloat16, T=8, Hq=24, Hk=4, D=256, rot=64, layout=0,
+                         w_mean=0.0, w_std=0.05, offset=1, theta=1e7, P=32768, positions="offset"),
+    "cfg3_16_2_T333": dict(dtype=torch.bfloat16, T=333, Hq=16, Hk=2, D=256, rot=64, layout=0,
+                           w_mean=0.0, w_std=0.05, offset=1, theta=1e7, P=32768,
+                           positions="offset"),
+    # workload 4: interleaved full rotary, direct weights, in place, fp16 and bf16
+    "cfg4_f16": dict(dtype=torch.float16, T=512, Hq=16, Hk=8, D=256, rot=256, layout=1,
+                     w_mean=1.0, w_std=0.02, offset=0, theta=1e6, P=4096, positions="arange",
+                     inplace=True),
+    "cfg4_bf16": dict(dtype=torch.bfloat16, T=512, Hq=16, Hk=8, D=256, rot=256, layout=1,
+                      w_mean=1.0, w_std=0.02, offset=0, theta=1e6, P=4096, positions="arange",
+                      inplace=True),
+    # head_dim 128 bf16: two heads per warp (half-warp lane groups)
+    "d128_bf16": dict(dtype=torch.bfloat16, T=37, Hq=16, Hk=8, D=128, rot=128, layout=0,
+                      w_mean=0.0, w_std=0.1, offset=1, theta=1e6, P=64,
+                      positions=np.r_[np.arange(30), [63, 64, 65, -1, -5, 1 << 40, 7]]),
+    "d64_f16_interleaved": dict(dtype=torch.float16, T=19, Hq=4, Hk=4, D=64, rot=32, layout=1,
+                                w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=32,
+                                positions="arange"),
+    # generic paths: non-power-of-two vectors per head, ragged rotary, odd sizes
+    "generic_d96": dict(dtype=torch.bfloat16, T=9, Hq=3, Hk=1, D=96, rot=96, layout=0,
+                        w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=16, positions="arange"),
+    "generic_rot24": dict(dtype=torch.bfloat16, T=5, Hq=4, Hk=2, D=256, rot=24, layout=0,
+                          w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=16, positions="arange"),
+    "generic_odd_d37": dict(dtype=torch.float16, T=6, Hq=2, Hk=3, D=37, rot=20, layout=1,
+                            w_mean=1.0, w_std=0.1, offset=0, theta=1e4, P=6,
+                            positions=np.array([0, 1, 2, 5, 6, -1])),
+    "generic_f32_d256": dict(dtype=torch.float32, T=7, Hq=4, Hk=2, D=256, rot=128, layout=0,
+                             w_mean=0.0, w_std=0.1, offset=1, theta=1e6, P=4096,
+                             positions="arange"),
+    "generic_misaligned": dict(dtype=torch.bfloat16, T=11, Hq=16, Hk=2, D=256, rot=64,
+                               layout=0, w_mean=0.0, w_std=0.05, offset=1, theta=1e7, P=4096,
+                               positions="offset", misalign=1),
+    "no_k_heads": dict(dtype=torch.bfloat16, T=3, Hq=8, Hk=0, D=128, rot=64, layout=0,
+                       w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=16, positions="arange"),
+    "no_rotation": dict(dtype=torch.bfloat16, T=4, Hq=8, Hk=2, D=128, rot=0, layout=0,
+                        w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=16, positions="arange"),
+    "no_weight": dict(dtype=torch.bfloat16, T=4, Hq=8, Hk=2, D=256, rot=64, layout=0,
+                      w_mean=None, w_std=0.0, offset=0, theta=1e7, P=64, positions="arange"),
+}
+
+
+def run_qk(c, fp8=False, seed=0, inv=None):
+    dtype, fmt = c["dtype"], TORCH_FMT[c["dtype"]]
+    inp = synth.qk_inputs(seed, dtype, c["T"], c["Hq"], c["Hk"], c["D"], c["rot"],
+                          theta=c["theta"], cache_len=c["P"], positions=c["positions"],
+                          w_mean=c["w_mean"] or 0.0, w_std=c["w_std"])
+    if c["w_mean"] is None:
+        inp["wq"] = inp["wk"] = None
+    out_fmt = oracle.E4M3 if fp8 else fmt
+    args = [storage(inp["q"]), storage(inp["k"]),
+            None if inp["wq"] is None else storage(inp["wq"]),
+            None if inp["wk"] is None else storage(inp["wk"]), fmt, c["rot"], c["layout"],
+            inp["positions"].numpy(), storage(inp["cos"]) if c["rot"] else None,
+            storage(inp["sin"]) if c["rot"] else None, 1e-6, c["offset"]]
+    if fp8 and inv is None:
+        cal = synth.qk_inputs(1, dtype, c["T"], c["Hq"], c["Hk"], c["D"], c["rot"],
+                              theta=c["theta"], cache_len=c["P"], positions=c["positions"],
+                              w_mean=c["w_mean"] or 0.0, w_std=c["w_std"])
+        cw = (None, None) if c["w_mean"] is None else (storage(cal["wq"]), storage(cal["wk"]))
+        rc = oracle.qk_norm_rope(storage(cal["q"]), storage(cal["k"]), *cw, *args[4:])
+        inv = calib_inv(np.concatenate([rc.q_pre.ravel(), rc.k_pre.ravel()]))
+    inv = 1.0 if inv is None else inv
+    ref = oracle.qk_norm_rope(*args, out_fmt=out_fmt, inv_scale=inv, eta=ETA_NORM)
+
+    mis = c.get("misalign", 0)
+    q, k = dev(inp["q"], mis), dev(inp["k"], mis)
+    wq, wk = dev(inp["wq"], mis), dev(inp["wk"], mis)
+    pos, cs, sn = dev(inp["positions"]), dev(inp["cos"]), dev(inp["sin"])
+    odt = torch.uint8 if fp8 else dtype
+    if c.get("inplace") and not fp8:
+        gq, gk = Guarded(q.shape, dtype), Guarded(k.shape, dtype)
+        gq.t.copy_(q)
+        gk.t.copy_(k)
+        q, k = gq.t, gk.t
+    else:
+        gq, gk = Guarded(q.shape, odt, mis), Guarded(k.shape, odt, mis)
+    edge_ops.qk_norm_rope(q, k, wq, wk, pos, cs, sn, rotary_dim=c["rot"], layout=c["layout"],
+                          eps=1e-6, weight_offset=c["offset"], q_out=gq.t, k_out=gk.t, fp8=fp8,
+                          inv_scale=inv, cache_len=c["P"])
+    torch.cuda.synchronize()
+    gq.check()
+    gk.check()
+    return ref, storage(gq.t.cpu()), storage(gk.t.cpu()), fmt, out_fmt, inv
+
+
+@pytest.mark.parametrize("name", list(QK_CASES))
+def test_qk_norm_rope(name):
+    c = QK_CASES[name]
+    ref, gq, gk, fmt, out_fmt, inv = run_qk(c)
+    check_out(name + " q", gq, ref.q_out, ref.q_pre, ref.q_mag, fmt, out_fmt, ETA_NORM,
+              alt=ref.q_alt)
+    if c["Hk"]:
+        check_out(name + " k", gk, ref.k_out, ref.k_pre, ref.k_mag, fmt, out_fmt, ETA_NORM,
+                  alt=ref.k_alt)
+
+
+@pytest.mark.parametrize("name", ["cfg3_16_2_T333", "cfg3_24_4_T8", "cfg4_bf16", "cfg1_f32",
+                                  "generic_odd_d37", "d128_bf16"])
+def test_qk_norm_rope_fp8(name):
+    c = dict(QK_CASES[name])
+    ref, gq, gk, fmt, out_fmt, inv = run_qk(c, fp8=True)
+    check_fp8_out(name + " q", gq, ref.q_pre, ref.q_mag, ETA_NORM, inv, alt=ref.q_alt)
+    check_fp8_out(name + " k", gk, ref.k_pre, ref.k_mag, ETA_NORM, inv, alt=ref.k_alt)
+
+
+@pytest.mark.parametrize("geom", [(16, 2), (24, 4)])
+@pytest.mark.parametrize("T", [256, 2048])
+def test_qk_text_profile_full_size(geom, T):
+    # workload 3 at its sweep sizes, in the launch configuration the benchmark times
+    c = dict(QK_CASES["cfg3_16_2_T1"], T=T, Hq=geom[0], Hk=geom[1])
+    ref, gq, gk, fmt, out_fmt, _ = run_qk(c)
+    check_out("q", gq, ref.q_out, ref.q_pre, ref.q_mag, fmt, out_fmt, ETA_NORM, alt=ref.q_alt)
+    check_out("k", gk, ref.k_out, ref.k_pre, ref.k_mag, fmt, out_fmt, ETA_NORM, alt=ref.k_alt)
+
+
+def test_qk_out_of_cache_token_untouched_by_rotation():
+    # the out-of-cache token of workload 1 equals the plain per-head RMSNorm
+    c = QK_CASES["cfg1_f32"]
+    ref, gq, gk, fmt, _, _ = run_qk(c)
+    inp = synth.qk_inputs(0, c["dtype"], c["T"], c["Hq"], c["Hk"], c["D"], c["rot"],
+                          theta=c["theta"], cache_len=c["P"], positions=c["positions"],
+                          w_mean=0.0, w_std=0.1)
+    x = dev(inp["q"][-1])
+    norm = edge_ops.rmsnorm(x, dev(inp["wq"]), eps=1e-6, weight_offset=1)
+    torch.cuda.synchronize()
+    ok = f32_ok(storage(norm.cpu()), ref.q_pre[-1], ref.q_mag[-1], 2e-6)
+    assert ok.all()
+    okq = f32_ok(gq[-1], ref.q_pre[-1], ref.q_mag[-1], 2e-6)
+    assert okq.all()
+
+
+# ---------------------------------------------------------------- rows
+
+ROW_CASES = {
+    # workload 2: decode residual-add RMSNorm, bf16, Llama and Gemma weights
+    "cfg2_h2560_T1_direct": dict(dtype=torch.bfloat16, T=1, H=2560, w_mean=1.0, w_std=0.02, off=0),
+    "cfg2_h2560_T4_offset": dict(dtype=torch.bfloat16, T=4, H=2560, w_mean=0.0, w_std=0.02, off=1),
+    "cfg2_h1024_T16_direct": dict(dtype=torch.bfloat16, T=16, H=1024, w_mean=1.0, w_std=0.02, off=0),
+    "cfg2_h1024_T64_offset": dict(dtype=torch.bfloat16, T=64, H=1024, w_mean=0.0, w_std=0.02, off=1),
+    "cfg2_h2560_T64_direct": dict(dtype=torch.bfloat16, T=64, H=2560, w_mean=1.0, w_std=0.02, off=0),
+    # workload 5 shapes in the activation dtype (the FP8 forms are below)
+    "h2048_T512": dict(dtype=torch.bfloat16, T=512, H=2048, w_mean=1.0, w_std=0.02, off=0,
+                       outliers=0.001),
+    "h2560_T700_ragged": dict(dtype=torch.bfloat16, T=700, H=2560, w_mean=0.0, w_std=0.02, off=1),
+    "f16_h1024_T33": dict(dtype=torch.float16, T=33, H=1024, w_mean=1.0, w_std=0.02, off=0),
+    "f32_h2048_T9": dict(dtype=torch.float32, T=9, H=2048, w_mean=0.0, w_std=0.1, off=1),
+    "f32_h4096_T300": dict(dtype=torch.float32, T=300, H=4096, w_mean=1.0, w_std=0.1, off=0),
+    "h16384_T3": dict(dtype=torch.bfloat16, T=3, H=16384, w_mean=1.0, w_std=0.1, off=0),
+    "generic_h37": dict(dtype=torch.bfloat16, T=64, H=37, w_mean=1.0, w_std=0.1, off=0),
+    "generic_f16_h1000_misaligned": dict(dtype=torch.float16, T=5, H=1000, w_mean=0.0,
+                                         w_std=0.1, off=1, misalign=1),
+    "generic_h40000": dict(dtype=torch.bfloat16, T=2, H=40000, w_mean=1.0, w_std=0.1, off=0),
+    "no_weight_h2048": dict(dtype=torch.bfloat16, T=128, H=2048, w_mean=None, w_std=0.0, off=0),
+}
+
+
+def run_rows(c, fused, fp8=False, inplace=False, seed=0):
+    dtype, fmt = c["dtype"], TORCH_FMT[c["dtype"]]
+    mk = lambda s: synth.rows_inputs(s, dtype, c["T"], c["H"], w_mean=c["w_mean"] or 0.0,
+                                     w_std=c["w_std"], outlier_frac=c.get("outliers", 0.0))
+    inp = mk(seed)
+    w = None if c["w_mean"] is None else inp["w"]
+    ws = None if w is None else storage(w)
+    out_fmt = oracle.E4M3 if fp8 else fmt
+    inv = 1.0
+    if fp8:
+        cal = mk(1)
+        if fused:
+            _, _, pre = oracle.add_rmsnorm(storage(cal["x"]), storage(cal["residual"]), ws, fmt,
+                                           1e-6, c["off"])
+        else:
+            _, pre = oracle.rmsnorm(storage(cal["x"]), ws, fmt, 1e-6, c["off"])
+        inv = calib_inv(pre)
+    if fused:
+        ref_out, ref_res, pre = oracle.add_rmsnorm(storage(inp["x"]), storage(inp["residual"]),
+                                                   ws, fmt, 1e-6, c["off"], out_fmt, inv)
+    else:
+        ref_out, pre = oracle.rmsnorm(storage(inp["x"]), ws, fmt, 1e-6, c["off"], out_fmt, inv)
+        ref_res = None
+    mis = c.get("misalign", 0)
+    x, wd = dev(inp["x"], mis), dev(w, mis)
+    odt = torch.uint8 if fp8 else dtype
+    if inplace:
+        g = Guarded(x.shape, dtype)
+        g.t.copy_(x)
+        x = g.t
+    else:
+        g = Guarded(x.shape, odt, mis)
+    gr = None
+    if fused:
+        gr = Guarded(x.shape, dtype, mis)
+        gr.t.copy_(dev(inp["residual"]))
+        edge_ops.add_rmsnorm(x, gr.t, wd, eps=1e-6, weight_offset=c["off"], out=g.t, fp8=fp8,
+                             inv_scale=inv)
+    else:
+        edge_ops.rmsnorm(x, wd, eps=1e-6, weight_offset=c["off"], out=g.t, fp8=fp8,
+                         inv_scale=inv)
+    torch.cuda.synchronize()
+    g.check()
+    if gr is not None:
+        gr.check()
+        assert np.array_equal(storage(gr.t.cpu()), ref_res), "residual sum not bit-exact"
+    got = storage(g.t.cpu())
+    check_out("out", got, ref_out, pre, np.abs(pre), fmt, out_fmt, ETA_NORM, inv)
+
+
+@pytest.mark.parametrize("name", list(ROW_CASES))
+@pytest.mark.parametrize("fused", [True, False])
+def test_rows(name, fused):
+    run_rows(ROW_CASES[name], fused)
+
+
+@pytest.mark.parametrize("name", ["cfg2_h2560_T4_offset", "h2048_T512", "generic_h37"])
+@pytest.mark.parametrize("fused", [True, False])
+def test_rows_in_place(name, fused):
+    c = ROW_CASES[name]
+    if c.get("misalign"):
+        pytest.skip("in-place case uses aligned buffers")
+    run_rows(c, fused, inplace=True)
+
+
+FP8_ROWS = {
+    # workload 5: bf16 in, FP8 out, D in {2048, 1024}, T=512, 0.1% outliers x20
+    "cfg5_d2048_w": dict(dtype=torch.bfloat16, T=512, H=2048, w_mean=1.0, w_std=0.02, off=0,
+                         outliers=0.001),
+    "cfg5_d1024_w": dict(dtype=torch.bfloat16, T=512, H=1024, w_mean=0.0, w_std=0.02, off=1,
+                         outliers=0.001),
+    "cfg5_d2048_noweight": dict(dtype=torch.bfloat16, T=512, H=2048, w_mean=None, w_std=0.0,
+                                off=0, outliers=0.001),
+    "cfg5_d1024_noweight_T4096": dict(dtype=torch.bfloat16, T=4096, H=1024, w_mean=None,
+                                      w_std=0.0, off=0, outliers=0.001),
+    "cfg5_d2048_T1": dict(dtype=torch.bfloat16, T=1, H=2048, w_mean=None, w_std=0.0, off=0,
+                          outliers=0.001),
+    "f32_h1024": dict(dtype=torch.float32, T=77, H=1024, w_mean=1.0, w_std=0.1, off=0),
+    "generic_h37": dict(dtype=torch.bfloat16, T=64, H=37, w_mean=1.0, w_std=0.1, off=0),
+}
+
+
+@pytest.mark.parametrize("name", list(FP8_ROWS))
+@pytest.mark.parametrize("fused", [True, False])
+def test_rows_fp8(name, fused):
+    run_rows(FP8_ROWS[name], fused, fp8=True)
+
+
+# ---------------------------------------------------------------- gates
+
+GLU_CASES = {
+    # workload 2: decode gates [T, 2*9728], bf16, N(0,1)
+    "cfg2_T1": dict(dtype=torch.bfloat16, T=1, d=9728, std=1.0),
+    "cfg2_T4": dict(dtype=torch.bfloat16, T=4, d=9728, std=1.0),
+    "cfg2_T64": dict(dtype=torch.bfloat16, T=64, d=9728, std=1.0),
+    # workload 4: prefill gates, N(0,2), fp16 and bf16
+    "cfg4_f16_I6912_T128": dict(dtype=torch.float16, T=128, d=6912, std=2.0),
+    "cfg4_bf16_I10240_T512": dict(dtype=torch.bfloat16, T=512, d=10240, std=2.0),
+    "cfg4_f16_I10240_T512": dict(dtype=torch.float16, T=512, d=10240, std=2.0),
+    "f32_accurate": dict(dtype=torch.float32, T=33, d=1024, std=3.0),
+    "generic_d37": dict(dtype=torch.bfloat16, T=21, d=37, std=2.0),
+    "generic_misaligned": dict(dtype=torch.float16, T=7, d=1000, std=2.0, misalign=1),
+    "wide_tail": dict(dtype=torch.bfloat16, T=3, d=8 * 1000 + 8, std=1.0),
+}
+
+
+def gate_eta(g, act):
+    g = g.astype(np.float64)
+    if act == oracle.SILU:
+        return (10.0 + 2.0 * np.abs(g)) * U
+    v = 2.0 * math.sqrt(2.0 / math.pi) * (g + 0.044715 * g ** 3)
+    return (10.0 + 5.0 * np.abs(v)) * U
+
+
+def run_glu(c, act, fp8=False, seed=0):
+    dtype, fmt = c["dtype"], TORCH_FMT[c["dtype"]]
+    mk = lambda s: synth.glu_inputs(s, dtype, c["T"], c["d"], std=c["std"],
+                                    outlier_frac=c.get("outliers", 0.0))
+    inp = mk(seed)
+    out_fmt = oracle.E4M3 if fp8 else fmt
+    inv = 1.0
+    if fp8:
+        _, pre = oracle.glu_act(storage(mk(1)["gate_up"]), fmt, act)
+        inv = calib_inv(pre)
+    ref, pre = oracle.glu_act(storage(inp["gate_up"]), fmt, act, out_fmt, inv)
+    mis = c.get("misalign", 0)
+    gu = dev(inp["gate_up"], mis)
+    g = Guarded((c["T"], c["d"]), torch.uint8 if fp8 else dtype, mis)
+    edge_ops.glu_act(gu, act, out=g.t, fp8=fp8, inv_scale=inv)
+    torch.cuda.synchronize()
+    g.check()
+    gate = oracle.decode(storage(inp["gate_up"]), fmt)[:, :c["d"]]
+    eta = gate_eta(gate, act)
+    check_out("glu", storage(g.t.cpu()), ref, pre, np.abs(pre), fmt, out_fmt, eta, inv)
+
+
+@pytest.mark.parametrize("name", list(GLU_CASES))
+@pytest.mark.parametrize("act", [oracle.SILU, oracle.GELU_TANH])
+def test_glu(name, act):
+    run_glu(GLU_CASES[name], act)
+
+
+FP8_GLU = {
+    # workload 5: GELU-tanh gate [T, 2D] with FP8 output, D in {2048, 1024}, T=512
+    "cfg5_d2048": dict(dtype=torch.bfloat16, T=512, d=2048, std=1.0, outliers=0.001),
+    "cfg5_d1024": dict(dtype=torch.bfloat16, T=512, d=1024, std=1.0, outliers=0.001),
+    "cfg5_d2048_T4096": dict(dtype=torch.bfloat16, T=4096, d=2048, std=1.0, outliers=0.001),
+    "generic_d37": dict(dtype=torch.bfloat16, T=21, d=37, std=2.0),
+    "f32_d256": dict(dtype=torch.float32, T=9, d=256, std=2.0),
+}
+
+
+@pytest.mark.parametrize("name", list(FP8_GLU))
+@pytest.mark.parametrize("act", [oracle.SILU, oracle.GELU_TANH])
+def test_glu_fp8(name, act):
+    run_glu(FP8_GLU[name], act, fp8=True)
+
+
+# ---------------------------------------------------------------- misc
+
+def test_invalid_call_raises_and_launches_nothing():
+    x = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    # an FP8 output cannot be written in place over its input
+    with pytest.raises(edge_ops.EdgeError, match="ALIAS"):
+        edge_ops.rmsnorm(x, None, out=x, fp8=True, inv_scale=1.0)
+    assert torch.count_nonzero(x) == 0
+
+
+def test_runs_on_a_side_stream_and_in_a_cuda_graph():
+    c = QK_CASES["cfg3_24_4_T8"]
+    inp = synth.qk_inputs(0, torch.bfloat16, 8, 24, 4, 256, 64, theta=1e7, cache_len=32768,
+                          positions="offset", w_std=0.05)
+    q, k, wq, wk = (dev(inp[n]) for n in ("q", "k", "wq", "wk"))
+    pos, cs, sn = dev(inp["positions"]), dev(inp["cos"]), dev(inp["sin"])
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    ref_q, ref_k = edge_ops.qk_norm_rope(q, k, wq, wk, pos, cs, sn, rotary_dim=64,
+                                         weight_offset=1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        edge_ops.qk_norm_rope(q, k, wq, wk, pos, cs, sn, rotary_dim=64, weight_offset=1,
+                              q_out=qo, k_out=ko)
+    torch.cuda.synchronize()
+    assert torch.equal(qo, ref_q) and torch.equal(ko, ref_k)
+    qo.zero_()
+    ko.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        edge_ops.qk_norm_rope(q, k, wq, wk, pos, cs, sn, rotary_dim=64, weight_offset=1,
+                              q_out=qo, k_out=ko)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(qo, ref_q) and torch.equal(ko, ref_k)
+    assert c["T"] == 8

@@ -65,6 +65,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["edge", "reference"], default="edge")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-t1", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -168,6 +169,23 @@ def visible_index(local_rank):
         if local_rank < len(ids) and ids[local_rank].isdigit():
             return int(ids[local_rank])
     return local_rank
+
+
+def reduce_max(v, world, device):
+    """The slowest rank's value (all ranks get it); the identity on one rank."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(step_bytes, steps, world, ms):
+    """Whole-job GB/s: every rank's algorithmic bytes over the slowest rank's time."""
+    return step_bytes * steps * world / (ms * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -289,12 +307,13 @@ def build_layers(torch, synth, device, seed):
 
 
 OPS = ("add_rmsnorm_in", "qk_norm_rope", "add_rmsnorm_post", "glu_silu")
-OP_BYTES = {"add_rmsnorm_in": bytes_add_rmsnorm(T_DEC, HID),
-            "qk_norm_rope": bytes_qk(T_DEC, HQ, HK, HD, HD),
-            "add_rmsnorm_post": bytes_add_rmsnorm(T_DEC, HID),
-            "glu_silu": bytes_glu(T_DEC, INTER)}
-OP_KERNEL = {"add_rmsnorm_in": "rows_vec_kernel", "qk_norm_rope": "qk_vec_kernel",
-             "add_rmsnorm_post": "rows_vec_kernel", "glu_silu": "glu_vec_kernel"}
+KERNEL_OPS = {"rows_vec_kernel": ("add_rmsnorm_in", "add_rmsnorm_post"),
+              "qk_vec_kernel": ("qk_norm_rope",), "glu_vec_kernel": ("glu_silu",)}
+# algorithmic bytes of one launch of each kernel in the step (both row-norm
+# launches of a layer move the same bytes)
+KERNEL_BYTES = {"rows_vec_kernel": bytes_add_rmsnorm(T_DEC, HID),
+                "qk_vec_kernel": bytes_qk(T_DEC, HQ, HK, HD, HD),
+                "glu_vec_kernel": bytes_glu(T_DEC, INTER)}
 OP_SOURCE = {"rows_vec_kernel": "rows.cu", "qk_vec_kernel": "qk_norm_rope.cu",
              "glu_vec_kernel": "glu.cu"}
 
@@ -310,6 +329,14 @@ def layer_ops(ops, L, sh):
                                                      out=L.h2)),
         ("glu_silu", lambda: ops.glu_act(L.gate_up, ops.SILU, out=L.act)),
     ]
+
+
+def graph_event(torch):
+    """A timing event that records a timestamp node when captured in a graph."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
 
 
 def capture(torch, fn, stream):
@@ -346,30 +373,50 @@ def traffic_for(kernel):
 # ---------------------------------------------------------------- sweep
 
 def sweep(torch, ops, synth, device, peak):
-    """Per-op device time vs T with a cold L2: an L2-sized write separates
-    every timed launch, and events bracket the launch alone (median of 15)."""
+    """Per-op time vs T.  S copies of the call's buffers, with S * bytes over
+    2.5x L2 where that fits in 64 copies, are cycled by a graph of at least 32
+    back-to-back launches, so every launch reads cold inputs from HBM.  The
+    graph is replayed 10 times after 3 warm-ups and timed with events.  Below
+    that size the data stays L2-resident, and the entry is marked warm."""
     bf = torch.bfloat16
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
     out = {}
 
-    def time_cold(fn, reps=15):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(reps)]
+    def timed(make, nbytes):
+        sets = int(min(64, max(2, -(-int(2.5 * L2_BYTES) // nbytes))))
+        fns = [make() for _ in range(sets)]
+        reps = sets * max(1, -(-32 // sets))
+
+        def body():
+            for i in range(reps):
+                fns[i % sets]()
+        g = capture(torch, body, stream)
+        for _ in range(3):
+            g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            fn()
-            for a, b in evs:
-                flush.fill_(1.0)
-                a.record(stream)
-                fn()
-                b.record(stream)
+            a.record(stream)
+            for _ in range(10):
+                g.replay()
+            b.record(stream)
         torch.cuda.synchronize()
-        return float(np.median([a.elapsed_time(b) for a, b in evs])) * 1e3  # us
-
-    def entry(us, nbytes):
+        us = a.elapsed_time(b) * 1e3 / (10 * reps)
         gbs = nbytes / (us * 1e-6) / 1e9
-        return [round(us, 3), round(gbs, 1), round(gbs / peak, 4)]
+        cold = sets * nbytes >= 2 * L2_BYTES
+        del g, fns
+        return [round(us, 3), round(gbs, 1), round(gbs / peak, 4), "cold" if cold else "warm"]
 
+    # reference: torch's own device copy under the same method (read + write bytes)
+    out["torch_copy_reference"] = {}
+    for mb in (16, 64, 256):
+        n = mb * 2 ** 20 // 2
+        src0 = torch.randn(n, device=device, dtype=bf)
+
+        def make(src0=src0):
+            a, b = src0.clone(), torch.empty_like(src0)
+            return lambda: b.copy_(a)
+        out["torch_copy_reference"][f"{mb}MB"] = timed(make, 2 * n * 2)
+        del src0
     # QK-norm+RoPE, text profile (head_dim 256, rotary 64, out of place)
     for (hq, hk) in ((16, 2), (24, 4)):
         key = f"qk_norm_rope_bf16_{hq}x{hk}_d256_r64"
@@ -378,40 +425,52 @@ def sweep(torch, ops, synth, device, peak):
             i = synth.qk_inputs(0, bf, T, hq, hk, 256, 64, theta=1e7, cache_len=32768,
                                 positions="offset", w_std=0.05)
             d = {k: v.to(device) for k, v in i.items()}
-            qo, ko = torch.empty_like(d["q"]), torch.empty_like(d["k"])
-            fn = lambda: ops.qk_norm_rope(d["q"], d["k"], d["wq"], d["wk"], d["positions"],
-                                          d["cos"], d["sin"], rotary_dim=64, weight_offset=1,
-                                          q_out=qo, k_out=ko)
-            out[key][str(T)] = entry(time_cold(fn), bytes_qk(T, hq, hk, 256, 64))
-    # residual-add RMSNorm, bf16 out and FP8 out, and the no-weight FP8 RMSNorm
+
+            def make(d=d):
+                q, k = d["q"].clone(), d["k"].clone()
+                qo, ko = torch.empty_like(q), torch.empty_like(k)
+                return lambda: ops.qk_norm_rope(q, k, d["wq"], d["wk"], d["positions"], d["cos"],
+                                                d["sin"], rotary_dim=64, weight_offset=1,
+                                                q_out=qo, k_out=ko)
+            out[key][str(T)] = timed(make, bytes_qk(T, hq, hk, 256, 64))
+    # residual-add RMSNorm, bf16 out and FP8 out
     for H in (2048, 1024, 2560):
         for fp8 in (False, True):
             key = f"add_rmsnorm_bf16_h{H}" + ("_fp8" if fp8 else "")
             out[key] = {}
             for T in (1, 16, 64, 256, 512, 1024, 4096):
                 i = synth.rows_inputs(0, bf, T, H)
-                x, r, w = (i[k].to(device) for k in ("x", "residual", "w"))
-                o = torch.empty(T, H, dtype=torch.uint8 if fp8 else bf, device=device)
-                fn = lambda: ops.add_rmsnorm(x, r, w, eps=EPS, out=o, fp8=fp8, inv_scale=40.0)
-                out[key][str(T)] = entry(time_cold(fn), bytes_add_rmsnorm(T, H, out_s=1 if fp8 else 2))
+                x0, r0, w = (i[k].to(device) for k in ("x", "residual", "w"))
+
+                def make(x0=x0, r0=r0, w=w, T=T, H=H, fp8=fp8):
+                    x, r = x0.clone(), r0.clone()
+                    o = torch.empty(T, H, dtype=torch.uint8 if fp8 else bf, device=device)
+                    return lambda: ops.add_rmsnorm(x, r, w, eps=EPS, out=o, fp8=fp8,
+                                                   inv_scale=40.0)
+                out[key][str(T)] = timed(make, bytes_add_rmsnorm(T, H, out_s=1 if fp8 else 2))
     key = "rmsnorm_noweight_bf16_h2048_fp8"
     out[key] = {}
     for T in (1, 64, 512, 4096):
-        i = synth.rows_inputs(0, bf, T, 2048, residual=False)
-        x = i["x"].to(device)
-        o = torch.empty(T, 2048, dtype=torch.uint8, device=device)
-        fn = lambda: ops.rmsnorm(x, None, eps=EPS, out=o, fp8=True, inv_scale=40.0)
-        out[key][str(T)] = entry(time_cold(fn), bytes_rmsnorm(T, 2048, out_s=1, weight=False))
+        x0 = synth.rows_inputs(0, bf, T, 2048, residual=False)["x"].to(device)
+
+        def make(x0=x0, T=T):
+            x = x0.clone()
+            o = torch.empty(T, 2048, dtype=torch.uint8, device=device)
+            return lambda: ops.rmsnorm(x, None, eps=EPS, out=o, fp8=True, inv_scale=40.0)
+        out[key][str(T)] = timed(make, bytes_rmsnorm(T, 2048, out_s=1, weight=False))
     # gates
     for name, d_, act, fp8 in (("glu_silu_bf16_d9728", INTER, ops.SILU, False),
-                               ("glu_gelu_bf16_d2048_fp8", 2048, ops.GELU_TANH, True)):
+                               ("glu_gelu_bf16_d2048_fp8", 2048, ops.GELU_TANH, True),
+                               ("glu_gelu_bf16_d10240", 10240, ops.GELU_TANH, False)):
         out[name] = {}
         for T in (1, 64, 512, 4096):
-            gu = synth.glu_inputs(0, bf, T, d_)["gate_up"].to(device)
-            o = torch.empty(T, d_, dtype=torch.uint8 if fp8 else bf, device=device)
-            fn = lambda: ops.glu_act(gu, act, out=o, fp8=fp8, inv_scale=40.0)
-            out[name][str(T)] = entry(time_cold(fn), bytes_glu(T, d_, out_s=1 if fp8 else 2))
-    del flush
+            gu0 = synth.glu_inputs(0, bf, T, d_)["gate_up"].to(device)
+
+            def make(gu0=gu0, T=T, d_=d_, act=act, fp8=fp8):
+                gu = gu0.clone()
+                o = torch.empty(T, d_, dtype=torch.uint8 if fp8 else bf, device=device)
+                return lambda: ops.glu_act(gu, act, out=o, fp8=fp8, inv_scale=40.0)
+            out[name][str(T)] = timed(make, bytes_glu(T, d_, out_s=1 if fp8 else 2))
     return out
 
 
@@ -493,11 +552,7 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world, device)
 
     layers, sh = build_layers(torch, synth, device, seed=rank)
     stream = torch.cuda.Stream(device)
@@ -511,20 +566,16 @@ def main():
     launches_per_step = LAYERS * len(OPS)
     step_bytes = LAYERS * layer_bytes()
 
-    # per-kernel breakdown: the same step with an event between launches
-    marks = []
-
-    def step_marked():
-        for L in layers:
-            for name, fn in layer_ops(ops, L, sh):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn()
-                b.record()
-                marks.append((name, a, b))
-
-    graph_marked = capture(torch, step_marked, stream)
-    marks = marks[len(marks) // 2:]  # the events recorded during capture (second call)
+    # per-kernel graphs: every launch of one kernel in a step, in step order,
+    # on the same per-layer buffers; timed over K replays like the step
+    kernel_graphs = {}
+    for kern, names in KERNEL_OPS.items():
+        def only(names=names):
+            for L in layers:
+                for name, fn in layer_ops(ops, L, sh):
+                    if name in names:
+                        fn()
+        kernel_graphs[kern] = capture(torch, only, stream)
 
     sampler = ClockSampler(visible_index(local)) if rank == 0 else None
     if sampler:
@@ -546,14 +597,21 @@ def main():
     t_wall1 = time.time()
     ms = max_over_ranks(e0.elapsed_time(e1))
 
-    # ---- per-kernel durations over K replays of the marked step
-    per_op = {n: [] for n in OPS}
-    reps = max(1, min(args.steps, 200))
-    for _ in range(reps):
-        graph_marked.replay()
-        torch.cuda.synchronize()
-        for name, a, b in marks:
-            per_op[name].append(a.elapsed_time(b))
+    # ---- per-kernel average launch duration: K replays of each kernel's graph
+    kernel_us = {}
+    for kern, g in kernel_graphs.items():
+        for _ in range(max(1, args.warmup)):
+            g.replay()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            b.record(stream)
+        barrier()
+        n = args.steps * LAYERS * len(KERNEL_OPS[kern])
+        kernel_us[kern] = max_over_ranks(a.elapsed_time(b)) * 1e3 / n
     if sampler:
         sampler.stop()
 
@@ -593,23 +651,22 @@ def main():
             dist.destroy_process_group()
         return 0
 
-    total_bytes = step_bytes * args.steps * world
-    value = total_bytes / (ms * 1e-3) / 1e9
-    e2e_value = step_bytes * e2e_steps * world / (e2e_ms * 1e-3) / 1e9
+    value = weak_scaling_value(step_bytes, args.steps, world, ms)
+    e2e_value = weak_scaling_value(step_bytes, e2e_steps, world, e2e_ms)
 
-    # dominant kernel: the largest share of the marked step's device time
-    op_ms = {n: float(np.sum(v)) for n, v in per_op.items()}
-    dom = max(op_ms, key=op_ms.get)
-    dom_launches = [x for x in per_op[dom]]
-    avg_us = float(np.mean(dom_launches)) * 1e3
-    achieved = OP_BYTES[dom] / (avg_us * 1e-6) / 1e9
-    kern = OP_KERNEL[dom]
-    roofline = {"bound": "hbm", "kernel": kern, "op": dom, "achieved": round(achieved, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+    # dominant kernel: the largest share of the step's device time
+    kern_ms = {k: kernel_us[k] * LAYERS * len(KERNEL_OPS[k]) for k in KERNEL_OPS}
+    dom = max(kern_ms, key=kern_ms.get)
+    avg_us = kernel_us[dom]
+    dom_bytes = KERNEL_BYTES[dom]
+    achieved = dom_bytes / (avg_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)",
-                "traffic": traffic_for(kern),
-                "bytes_per_launch": OP_BYTES[dom], "avg_launch_us": round(avg_us, 3),
-                "share": {n: round(op_ms[n] / sum(op_ms.values()), 4) for n in OPS}}
+                "traffic": traffic_for(dom), "bytes_per_launch": dom_bytes,
+                "avg_launch_us": round(avg_us, 3),
+                "launch_us": {k: round(v, 3) for k, v in kernel_us.items()},
+                "share": {k: round(v / sum(kern_ms.values()), 4) for k, v in kern_ms.items()}}
 
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else {}
     line = {
@@ -624,6 +681,7 @@ def main():
                    "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB per step, "
                          "distinct buffers per layer",
                    "graph": "one CUDA graph per step (144 launches)",
+                   "pdl": os.environ.get("EDGE_OPS_PDL", "1") != "0",
                    "parallelism": f"replicas x{world}"},
         "step_bytes": step_bytes,
         "roofline": roofline,
@@ -633,10 +691,12 @@ def main():
         "clocks": clocks,
     }
     if world == 1:
-        line["t1_us_per_call"] = t1_latency(torch, ops, synth, device)
+        if not args.no_t1:
+            line["t1_us_per_call"] = t1_latency(torch, ops, synth, device)
         if not args.no_sweep:
             line["sweep"] = sweep(torch, ops, synth, device, peak)
-            line["sweep_format"] = "T -> [us per call (cold L2), GB/s, fraction of peak]"
+            line["sweep_format"] = ("T -> [us per call in back-to-back graph replay, GB/s, "
+                                    "fraction of measured HBM peak, L2 state]")
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -158,9 +158,71 @@ __device__ __forceinline__ float group_sum(float v) {
     return v;
 }
 
-// 1 / sqrt(ss / n + eps) with correctly rounded divide and square root.
-__device__ __forceinline__ float inv_rms(float ss, float n, float eps) {
-    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), eps)));
+// 1 / sqrt(ss / n + eps), with inv_n = 1/n rounded to fp32 on the host and
+// the hardware reciprocal square root (rsqrtf, at most 2 ulp).  Its relative
+// error, a few fp32 ulps, is far inside the tolerance band of every output.
+__device__ __forceinline__ float inv_rms(float ss, float inv_n, float eps) {
+    return rsqrtf(__fmaf_rn(ss, inv_n, eps));
+}
+
+// ---------------------------------------------------------------- bulk copies
+
+// Shared-memory address of a generic pointer into this CTA's shared memory.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialization visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared accesses before later
+// bulk copies into the same shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// One bulk copy global -> this CTA's shared memory (16-byte aligned ends,
+// size a multiple of 16), completing on barrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for phase `parity` of barrier `bar`.  Returns false after
+// kSpinLimit polls (each poll may itself suspend for a short while); the
+// caller then records the failure instead of waiting forever.
+constexpr uint32_t kSpinLimit = 1u << 22;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+    }
+    return false;
 }
 
 // ---------------------------------------------------------------- PDL hooks

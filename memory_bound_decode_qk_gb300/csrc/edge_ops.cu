@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <atomic>
+#include <initializer_list>
 
 #include "../../include/edge_ops.h"
 #include "launch.h"
@@ -36,9 +37,34 @@ int sm_count() {
 bool pdl_enabled() {
     static const bool on = [] {
         const char* v = std::getenv("EDGE_OPS_PDL");
-        return v != nullptr && v[0] == '1';
+        return !(v != nullptr && v[0] == '0');
     }();
     return on;
+}
+
+static int env_choice(const char* name, std::initializer_list<int> allowed) {
+    const char* v = std::getenv(name);
+    if (v == nullptr) return 0;
+    const int n = std::atoi(v);
+    for (int a : allowed) {
+        if (a == n) return n;
+    }
+    return 0;
+}
+
+int qk_path_override() {
+    static const int v = env_choice("EDGE_OPS_QK_PATH", {1, 3});
+    return v;
+}
+
+int rows_vt_override() {
+    static const int v = env_choice("EDGE_OPS_ROWS_VT", {1, 2, 4, 8});
+    return v;
+}
+
+int glu_unroll_override() {
+    static const int v = env_choice("EDGE_OPS_GLU_UNROLL", {1, 2, 4});
+    return v;
 }
 
 }  // namespace edge

@@ -210,16 +210,23 @@ cudaError_t launch_typed(const GluArgs& a, GluP& p, cudaStream_t s) {
     const bool vec = (a.d * (int64_t)sizeof(T)) % 16 == 0 && aligned(a.gate_up, 16) &&
                      aligned(a.out, FP8 ? N : 16) && a.rows * dvec <= kMaxUnits;
     if (vec) {
-        constexpr int U = 2;
         p.dv = make_fastdiv((uint32_t)dvec);
         p.total = (uint32_t)(a.rows * dvec);
         const int threads = 256;
+        // one vector per thread and a one-shot grid (measured on GB300: 2 or 4
+        // vectors per thread were slower at every size)
+        int U = 1;
+        if (glu_unroll_override() > 0) U = glu_unroll_override();
         int64_t blocks = ((int64_t)p.total + threads * U - 1) / (threads * U);
-        const int64_t cap = (int64_t)sms * (2048 / threads) * 16;
+        const int64_t cap = (int64_t)sms * (2048 / threads) * 64;
         if (blocks > cap) blocks = cap;
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(threads);
-        return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, U>, p);
+        switch (U) {
+            case 1: return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, 1>, p);
+            case 2: return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, 2>, p);
+            default: return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, 4>, p);
+        }
     }
     const int64_t total = a.rows * a.d;
     int64_t blocks = (total + 255) / 256;

@@ -61,8 +61,19 @@ cudaError_t launch_glu(const GluArgs& a, cudaStream_t s);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
-// Programmatic dependent launch for all ops: EDGE_OPS_PDL=1 in the
-// environment, read once per process.
+// Programmatic dependent launch for all ops (on unless EDGE_OPS_PDL=0 in the
+// environment, read once per process).  Every kernel executes
+// griddepcontrol.wait before its first global access, so it is always safe as
+// a dependent; it triggers its own dependents at its start.
 bool pdl_enabled();
+
+// Launch-shape overrides for tuning (0: the built-in choice), read once from
+// EDGE_OPS_QK_PATH (1: one head per lane group, 3: four threads per head),
+// EDGE_OPS_ROWS_VT (target vectors per thread: 1, 2, 4 or 8) and
+// EDGE_OPS_GLU_UNROLL (vectors per thread: 1, 2 or 4).
+int qk_path_override();
+int rows_vt_override();
+int glu_unroll_override();
+
 
 }  // namespace edge

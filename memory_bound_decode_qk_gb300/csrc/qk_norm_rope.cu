@@ -21,63 +21,156 @@
 // Generic path: one warp per head, staged through shared memory.  It serves
 // any head_dim up to 2048, any even rotary_dim and any element-aligned
 // pointer.
-#include "edge_common.cuh"
-#include "fastdiv.h"
-#include "launch.h"
+#include "qk_common.cuh"
 
 namespace edge {
 namespace {
 
-constexpr int kRotateHalf = 0;
-constexpr int kInterleaved = 1;
+// ---------------------------------------------------------------- shared head math
 
-struct QKP {
-    const char* q;
-    const char* k;
-    char* qo;
-    char* ko;
-    const char* wq;
-    const char* wk;
-    const int64_t* pos;
-    const float* cs;
-    const float* sn;
-    int64_t cache_len;
-    uint32_t units;        // tokens * (q_heads + k_heads)
-    FastDiv heads;         // q_heads + k_heads
-    int q_heads, k_heads, D, rot, half;
-    int in_bytes, out_bytes;  // element sizes of input and output
-    float eps, delta, inv, fD;
+// Cache entries a lane needs: rotate-half lanes hold N consecutive channels of
+// one half (N entries); interleaved lanes hold N/2 pairs (N/2 entries).
+template <typename T, int LAYOUT>
+struct CacheRegs {
+    static constexpr int N = vec_elems<T>();
+    static constexpr int kCount = LAYOUT == kInterleaved ? N / 2 : N;
+    float c[kCount], s[kCount];
 };
 
-struct Unit {
-    const char* src;
-    char* dst;
-    const char* w;
-    int64_t t;
-};
-
-__device__ __forceinline__ Unit locate(const QKP& p, uint32_t u) {
-    uint32_t t = fast_div(u, p.heads);
-    int h = (int)(u - t * p.heads.d);
-    Unit r;
-    r.t = t;
-    int64_t row;
-    if (h < p.q_heads) {
-        row = (int64_t)t * p.q_heads + h;
-        r.src = p.q + row * p.D * p.in_bytes;
-        r.dst = p.qo + row * p.D * p.out_bytes;
-        r.w = p.wq;
+// Role of a lane's vector in the rotation: 0 none, 1 first member, 2 second.
+template <typename T, int LAYOUT>
+__device__ __forceinline__ int rotary_role(const QKP& p, int sub) {
+    constexpr int N = vec_elems<T>();
+    const int e0 = sub * N;
+    if constexpr (LAYOUT == kInterleaved) {
+        return e0 < p.rot ? 1 : 0;
     } else {
-        row = (int64_t)t * p.k_heads + (h - p.q_heads);
-        r.src = p.k + row * p.D * p.in_bytes;
-        r.dst = p.ko + row * p.D * p.out_bytes;
-        r.w = p.wk;
+        return e0 < p.half ? 1 : (e0 < p.rot ? 2 : 0);
     }
-    return r;
 }
 
-// ---------------------------------------------------------------- fast path
+// Load this lane's cos/sin entries of cache row `pos` (role != 0 only).
+template <typename T, int LAYOUT>
+__device__ __forceinline__ void load_cache(const QKP& p, int64_t pos, int sub, int role,
+                                           CacheRegs<T, LAYOUT>& cr) {
+    constexpr int N = vec_elems<T>();
+    const int e0 = sub * N;
+    if constexpr (LAYOUT == kInterleaved) {
+        const float* crow = p.cs + pos * p.half + e0 / 2;
+        const float* srow = p.sn + pos * p.half + e0 / 2;
+        if constexpr (N == 8) {
+            float4 c4 = __ldg(reinterpret_cast<const float4*>(crow));
+            float4 s4 = __ldg(reinterpret_cast<const float4*>(srow));
+            cr.c[0] = c4.x; cr.c[1] = c4.y; cr.c[2] = c4.z; cr.c[3] = c4.w;
+            cr.s[0] = s4.x; cr.s[1] = s4.y; cr.s[2] = s4.z; cr.s[3] = s4.w;
+        } else {
+            float2 c2 = __ldg(reinterpret_cast<const float2*>(crow));
+            float2 s2 = __ldg(reinterpret_cast<const float2*>(srow));
+            cr.c[0] = c2.x; cr.c[1] = c2.y;
+            cr.s[0] = s2.x; cr.s[1] = s2.y;
+        }
+    } else {
+        const int j0 = role == 1 ? e0 : e0 - p.half;
+        const float4* c4 = reinterpret_cast<const float4*>(p.cs + pos * p.half + j0);
+        const float4* s4 = reinterpret_cast<const float4*>(p.sn + pos * p.half + j0);
+#pragma unroll
+        for (int v = 0; v < N / 4; ++v) {
+            float4 cc = __ldg(c4 + v), sv = __ldg(s4 + v);
+            cr.c[4 * v] = cc.x; cr.c[4 * v + 1] = cc.y; cr.c[4 * v + 2] = cc.z; cr.c[4 * v + 3] = cc.w;
+            cr.s[4 * v] = sv.x; cr.s[4 * v + 1] = sv.y; cr.s[4 * v + 2] = sv.z; cr.s[4 * v + 3] = sv.w;
+        }
+    }
+}
 
+// Normalize, round to the dtype, rotate and store one head held as one
+// 16-byte vector per lane of an LPH-lane group.  w holds w + delta.  All 32
+// lanes of the warp call this together (the rotate-half partner comes over a
+// warp shuffle); inactive groups carry zeros and store nothing.  `role` is
+// this lane's rotation role for this head's token (0 when it does not rotate).
+template <typename T, bool FP8, int LPH, int LAYOUT>
+__device__ __forceinline__ void qk_core(const QKP& p, char* dst, bool active, int lane, int sub,
+                                        const uint4& raw, const float (&w)[vec_elems<T>()], int role,
+                                        const CacheRegs<T, LAYOUT>& cr) {
+    constexpr int N = vec_elems<T>();
+    float x[N];
+    unpack_vec<T, N>(raw, x);
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+    ss = group_sum<LPH>(ss);
+    const float r = inv_rms(ss, p.invD, p.eps);
+
+    // normalized value, rounded to the activation dtype before the rotation
+    float m[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) m[i] = round_to<T>(__fmul_rn(__fmul_rn(x[i], r), w[i]));
+
+    float y[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) y[i] = m[i];
+
+    if constexpr (LAYOUT == kInterleaved) {
+        if (role != 0) {
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                const float a = m[2 * i], b = m[2 * i + 1];
+                y[2 * i] = __fmaf_rn(a, cr.c[i], -__fmul_rn(b, cr.s[i]));
+                y[2 * i + 1] = __fmaf_rn(b, cr.c[i], __fmul_rn(a, cr.s[i]));
+            }
+        }
+    } else {
+        // rotate-half: channel e pairs with e + half; the partner vector is
+        // held by the lane half/N positions away in the same lane group
+        const int hv = p.half / N;
+        const int src = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
+        const uint4 mine = pack_vec<T, N>(m);  // exact: m is already rounded to T
+        uint4 other;
+        other.x = __shfl_sync(0xffffffffu, mine.x, src);
+        other.y = __shfl_sync(0xffffffffu, mine.y, src);
+        other.z = __shfl_sync(0xffffffffu, mine.z, src);
+        other.w = __shfl_sync(0xffffffffu, mine.w, src);
+        if (role != 0) {
+            float pm[N];
+            unpack_vec<T, N>(other, pm);
+            if (role == 1) {
+#pragma unroll
+                for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(m[i], cr.c[i], -__fmul_rn(pm[i], cr.s[i]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(m[i], cr.c[i], __fmul_rn(pm[i], cr.s[i]));
+            }
+        }
+    }
+
+    if (active) {
+        if constexpr (FP8) {
+            auto q8 = quantize_vec<N>(y, p.inv);
+            reinterpret_cast<decltype(q8)*>(dst)[sub] = q8;
+        } else {
+            reinterpret_cast<uint4*>(dst)[sub] = pack_vec<T, N>(y);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void weights_plus_delta(const QKP& p, const char* wptr, int sub,
+                                                   float (&w)[vec_elems<T>()]) {
+    constexpr int N = vec_elems<T>();
+    if (wptr != nullptr) {
+        uint4 wr = __ldg(reinterpret_cast<const uint4*>(wptr) + sub);
+        unpack_vec<T, N>(wr, w);
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = __fadd_rn(w[i], p.delta);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = 1.0f;
+    }
+}
+
+// ---------------------------------------------------------------- decode-width path
+
+// One head per lane group, a one-shot grid.  Every load of a head (data,
+// weight, position) is issued up front; the cache row follows the position.
 template <typename T, bool FP8, int LPH, int LAYOUT>
 __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
     constexpr int N = vec_elems<T>();
@@ -94,8 +187,7 @@ __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
     for (uint32_t base = warp * HPW; base < p.units; base += nwarps * HPW) {
         const uint32_t u = base + slot;
         const bool active = u < p.units;
-        Unit un = locate(p, active ? u : base);
-
+        const Unit un = locate(p, active ? u : base);
         uint4 raw = make_uint4(0u, 0u, 0u, 0u);
         int64_t pos = -1;
         if (active) {
@@ -103,103 +195,12 @@ __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
             if (p.rot > 0) pos = __ldg(p.pos + un.t);
         }
         float w[N];
-        if (un.w != nullptr) {
-            uint4 wr = __ldg(reinterpret_cast<const uint4*>(un.w) + sub);
-            unpack_vec<T, N>(wr, w);
-#pragma unroll
-            for (int i = 0; i < N; ++i) w[i] = __fadd_rn(w[i], p.delta);
-        } else {
-#pragma unroll
-            for (int i = 0; i < N; ++i) w[i] = 1.0f;
-        }
-
-        float x[N];
-        unpack_vec<T, N>(raw, x);
-        float ss = 0.0f;
-#pragma unroll
-        for (int i = 0; i < N; ++i) ss = __fmaf_rn(x[i], x[i], ss);
-        ss = group_sum<LPH>(ss);
-        const float r = inv_rms(ss, p.fD, p.eps);
-
-        // normalized value, rounded to the activation dtype before the rotation
-        float m[N];
-#pragma unroll
-        for (int i = 0; i < N; ++i) m[i] = round_to<T>(__fmul_rn(__fmul_rn(x[i], r), w[i]));
-
+        weights_plus_delta<T>(p, un.w, sub, w);
         const bool rot = active && pos >= 0 && pos < p.cache_len;
-        const int e0 = sub * N;  // first channel held by this lane
-        float y[N];
-#pragma unroll
-        for (int i = 0; i < N; ++i) y[i] = m[i];
-
-        if constexpr (LAYOUT == kInterleaved) {
-            if (rot && e0 < p.rot) {
-                // pairs (e0 + 2i, e0 + 2i + 1) use cache entries e0/2 + i
-                const float* crow = p.cs + pos * p.half + e0 / 2;
-                const float* srow = p.sn + pos * p.half + e0 / 2;
-                float c[N / 2], s[N / 2];
-                if constexpr (N == 8) {
-                    float4 c4 = __ldg(reinterpret_cast<const float4*>(crow));
-                    float4 s4 = __ldg(reinterpret_cast<const float4*>(srow));
-                    c[0] = c4.x; c[1] = c4.y; c[2] = c4.z; c[3] = c4.w;
-                    s[0] = s4.x; s[1] = s4.y; s[2] = s4.z; s[3] = s4.w;
-                } else {
-                    float2 c2 = __ldg(reinterpret_cast<const float2*>(crow));
-                    float2 s2 = __ldg(reinterpret_cast<const float2*>(srow));
-                    c[0] = c2.x; c[1] = c2.y;
-                    s[0] = s2.x; s[1] = s2.y;
-                }
-#pragma unroll
-                for (int i = 0; i < N / 2; ++i) {
-                    const float a = m[2 * i], b = m[2 * i + 1];
-                    y[2 * i] = __fmaf_rn(a, c[i], -__fmul_rn(b, s[i]));
-                    y[2 * i + 1] = __fmaf_rn(b, c[i], __fmul_rn(a, s[i]));
-                }
-            }
-        } else {
-            // rotate-half: channel e pairs with e + half; the partner vector is
-            // held by the lane half/N positions away in the same head group
-            const int hv = p.half / N;
-            int role = 0;  // 1: first member (a), 2: second member (b)
-            if (rot) role = e0 < p.half ? 1 : (e0 < p.rot ? 2 : 0);
-            const int src = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
-            const uint4 mine = pack_vec<T, N>(m);  // exact: m is already rounded to T
-            uint4 other;
-            other.x = __shfl_sync(0xffffffffu, mine.x, src);
-            other.y = __shfl_sync(0xffffffffu, mine.y, src);
-            other.z = __shfl_sync(0xffffffffu, mine.z, src);
-            other.w = __shfl_sync(0xffffffffu, mine.w, src);
-            if (role != 0) {
-                float pm[N];
-                unpack_vec<T, N>(other, pm);
-                const int j0 = role == 1 ? e0 : e0 - p.half;
-                const float4* c4 = reinterpret_cast<const float4*>(p.cs + pos * p.half + j0);
-                const float4* s4 = reinterpret_cast<const float4*>(p.sn + pos * p.half + j0);
-                float c[N], s[N];
-#pragma unroll
-                for (int v = 0; v < N / 4; ++v) {
-                    float4 cc = __ldg(c4 + v), sv = __ldg(s4 + v);
-                    c[4 * v] = cc.x; c[4 * v + 1] = cc.y; c[4 * v + 2] = cc.z; c[4 * v + 3] = cc.w;
-                    s[4 * v] = sv.x; s[4 * v + 1] = sv.y; s[4 * v + 2] = sv.z; s[4 * v + 3] = sv.w;
-                }
-                if (role == 1) {
-#pragma unroll
-                    for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(m[i], c[i], -__fmul_rn(pm[i], s[i]));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(m[i], c[i], __fmul_rn(pm[i], s[i]));
-                }
-            }
-        }
-
-        if (active) {
-            if constexpr (FP8) {
-                auto q8 = quantize_vec<N>(y, p.inv);
-                reinterpret_cast<decltype(q8)*>(un.dst)[sub] = q8;
-            } else {
-                reinterpret_cast<uint4*>(un.dst)[sub] = pack_vec<T, N>(y);
-            }
-        }
+        const int role = rot ? rotary_role<T, LAYOUT>(p, sub) : 0;
+        CacheRegs<T, LAYOUT> cr;
+        if (role != 0) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
+        qk_core<T, FP8, LPH, LAYOUT>(p, un.dst, active, lane, sub, raw, w, role, cr);
     }
 }
 
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(128) qk_generic_kernel(QKP p, int layout) {
             ss = __fmaf_rn(v, v, ss);
         }
         ss = group_sum<32>(ss);
-        const float r = inv_rms(ss, p.fD, p.eps);
+        const float r = inv_rms(ss, p.invD, p.eps);
         for (int e = lane; e < p.D; e += 32) {
             float w = un.w ? __fadd_rn(ld_elem<T>(un.w, e), p.delta) : 1.0f;
             hm[e] = round_to<T>(__fmul_rn(__fmul_rn(hm[e], r), w));
@@ -303,10 +304,21 @@ cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
     if (vec) {
         const int lph = nvec;
         const int hpw = 32 / lph;
+        int path = qk_path_override();
+        if (path == 0) path = qk_quad_preferred(a, sms) ? 3 : 1;
+        if (path == 3) {
+            bool handled = false;
+            cudaError_t e = launch_qk_quad<T, FP8>(a, p, cfg, &handled);
+            if (handled || e != cudaSuccess) return e;
+        }
+        // decode-width path: one head per lane group, a one-shot grid (on
+        // GB300 many short CTAs that each issue one round of loads keep more
+        // requests in flight than fewer, fatter warps: several heads in
+        // flight per group or a resident looping grid measured slower)
         const int threads = 256;
         const int64_t per_block = (int64_t)(threads / 32) * hpw;
         int64_t blocks = ((int64_t)p.units + per_block - 1) / per_block;
-        const int64_t cap = (int64_t)sms * (2048 / threads) * 8;
+        const int64_t cap = (int64_t)sms * (2048 / threads) * 64;
         if (blocks > cap) blocks = cap;
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(threads);
@@ -365,8 +377,12 @@ cudaError_t launch_qk(const QKArgs& args, cudaStream_t s) {
     p.cs = a.cos;
     p.sn = a.sin;
     p.cache_len = a.rotary_dim > 0 ? a.cache_len : 0;
+    p.tokens = a.tokens;
     p.units = (uint32_t)(a.tokens * (a.q_heads + a.k_heads));
     p.heads = make_fastdiv((uint32_t)(a.q_heads + a.k_heads));
+    p.qdiv = make_fastdiv((uint32_t)a.q_heads);
+    p.kdiv = make_fastdiv((uint32_t)(a.k_heads > 0 ? a.k_heads : 1));
+    p.qrows = (uint32_t)(a.tokens * a.q_heads);
     p.q_heads = a.q_heads;
     p.k_heads = a.k_heads;
     p.D = a.head_dim;
@@ -377,7 +393,7 @@ cudaError_t launch_qk(const QKArgs& args, cudaStream_t s) {
     p.eps = a.eps;
     p.delta = (float)a.weight_offset;
     p.inv = a.inv_scale;
-    p.fD = (float)a.head_dim;
+    p.invD = 1.0f / (float)a.head_dim;
     const bool fp8 = a.out_dt == kFP8;
     switch (a.dt) {
         case kF32:

@@ -35,7 +35,7 @@ struct RowsP {
     int nvec;      // 16-byte vectors per row
     int W;         // warps per row
     int RPB;       // rows per CTA
-    float eps, delta, inv, fH;
+    float eps, delta, inv, invH;  // invH = 1 / hidden (fp32)
 };
 
 template <typename T, bool FP8, bool ADD, int V>
@@ -60,13 +60,17 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
         const uint4* xr = reinterpret_cast<const uint4*>(p.x + rsafe * in_row);
         uint4* rr = ADD ? reinterpret_cast<uint4*>(p.res + rsafe * in_row) : nullptr;
 
-        uint4 xv[V], rv[V];
+        // every load of the row (x, residual and the weight) is issued before
+        // any arithmetic: one memory round trip per row
+        const uint4* wv = reinterpret_cast<const uint4*>(p.w);
+        uint4 xv[V], rv[V], wr[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int idx = tid + i * tpr;
             const bool ok = active && idx < p.nvec;
             xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
             if constexpr (ADD) rv[i] = ok ? __ldcs(rr + idx) : make_uint4(0u, 0u, 0u, 0u);
+            wr[i] = (ok && wv != nullptr) ? __ldg(wv + idx) : make_uint4(0u, 0u, 0u, 0u);
         }
 
         float ss = 0.0f;
@@ -95,9 +99,8 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
             for (int k = 0; k < p.W; ++k) ss = __fadd_rn(ss, red[g * p.W + k]);
             __syncthreads();
         }
-        const float r = inv_rms(ss, p.fH, p.eps);
+        const float r = inv_rms(ss, p.invH, p.eps);
 
-        const uint4* wv = reinterpret_cast<const uint4*>(p.w);
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int idx = tid + i * tpr;
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
             unpack_vec<T, N>(xv[i], s);
             if (wv != nullptr) {
                 float w[N];
-                unpack_vec<T, N>(__ldg(wv + idx), w);
+                unpack_vec<T, N>(wr[i], w);
 #pragma unroll
                 for (int e = 0; e < N; ++e) y[e] = __fmul_rn(__fmul_rn(s[e], r), __fadd_rn(w[e], p.delta));
             } else {
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(256) rows_generic_kernel(RowsP p) {
         ss = 0.0f;
         for (int k = 0; k < nw; ++k) ss = __fadd_rn(ss, red[k]);
         __syncthreads();
-        const float r = inv_rms(ss, p.fH, p.eps);
+        const float r = inv_rms(ss, p.invH, p.eps);
         const T* w = reinterpret_cast<const T*>(p.w);
         for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
             const float s = ADD ? to_f(res[i]) : to_f(x[i]);
@@ -189,7 +192,10 @@ cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
     if (vec_ok && nvec <= 16 * 32 * 8) {
         // vectors per thread: many rows -> more bytes in flight per thread;
         // few rows -> spread each row over more warps
-        const int vt = a.rows >= 2 * sms ? 4 : 2;
+        // target vectors per thread (measured on GB300: 1 for few rows, 2 for
+        // many; more per thread lowers occupancy and loses bandwidth)
+        int vt = a.rows >= 2 * sms ? 2 : 1;
+        if (rows_vt_override() > 0) vt = rows_vt_override();
         int W = (int)((nvec + 32 * vt - 1) / (32 * vt));
         if (W > 16) W = 16;
         const int64_t per = (nvec + 32 * W - 1) / (32 * W);
@@ -244,7 +250,7 @@ cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s) {
     p.eps = a.eps;
     p.delta = (float)a.weight_offset;
     p.inv = a.inv_scale;
-    p.fH = (float)a.hidden;
+    p.invH = 1.0f / (float)a.hidden;
     switch (a.dt) {
         case kF32: return launch_dt<float>(a, p, s);
         case kF16: return launch_dt<__half>(a, p, s);

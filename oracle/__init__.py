@@ -66,8 +66,8 @@ def _lib():
         L.oracle_add_rmsnorm.argtypes = [P, I, P, P, P, P, P, I, I64, I64, F, I, F]
         L.oracle_glu_act.argtypes = [P, I, P, P, I, I64, I64, I, F]
         L.oracle_rope.argtypes = [P, I, P, I, I64, I, I, I, I, P, P, P, I64]
-        L.oracle_qk_norm_rope.argtypes = [P, P, I, P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I,
-                                          I, I, P, P, P, I64, F, I, F, D]
+        L.oracle_qk_norm_rope.argtypes = [P, P, I, P, P, P, P, P, P, P, P, P, P, P, P, I, I64, I,
+                                          I, I, I, I, P, P, P, I64, F, I, F, D]
         L.oracle_set_rotation_scale.argtypes = [D]
         for name in ("oracle_rmsnorm", "oracle_add_rmsnorm", "oracle_glu_act", "oracle_rope",
                      "oracle_qk_norm_rope", "oracle_version"):
@@ -205,7 +205,12 @@ class QKResult:
 
 def qk_norm_rope(q, k, wq, wk, fmt, rotary_dim, layout, positions, cos, sin, eps,
                  weight_offset=0, out_fmt=None, inv_scale=1.0, eta=2.0 ** -20, cache_len=None):
-    """q: [T, Hq, D], k: [T, Hk, D] storage; cos/sin: [P, rotary_dim/2] fp32."""
+    """q: [T, Hq, D], k: [T, Hk, D] storage; cos/sin: [P, rotary_dim/2] fp32.
+
+    Besides the outputs, returns per element the exact pre-rounding value
+    (q_pre, k_pre), its bounds over the near-tie neighbours of the
+    intermediate roundings (q_lo/q_hi, k_lo/k_hi; band eta, relative) and the
+    error scale (q_mag, k_mag: the pair norm for rotated channels)."""
     out_fmt = fmt if out_fmt is None else out_fmt
     q = _c(q, STORAGE[fmt])
     k = _c(k, STORAGE[fmt])
@@ -221,11 +226,13 @@ def qk_norm_rope(q, k, wq, wk, fmt, rotary_dim, layout, positions, cos, sin, eps
     res = QKResult(
         q_out=np.empty(q.shape, STORAGE[out_fmt]), k_out=np.empty(k.shape, STORAGE[out_fmt]),
         q_pre=np.empty(q.shape), k_pre=np.empty(k.shape),
-        q_alt=np.empty(q.shape), k_alt=np.empty(k.shape),
+        q_lo=np.empty(q.shape), k_lo=np.empty(k.shape),
+        q_hi=np.empty(q.shape), k_hi=np.empty(k.shape),
         q_mag=np.empty(q.shape), k_mag=np.empty(k.shape))
     rc = _lib().oracle_qk_norm_rope(
         _ptr(res.q_out), _ptr(res.k_out), out_fmt, _ptr(res.q_pre), _ptr(res.k_pre),
-        _ptr(res.q_alt), _ptr(res.k_alt), _ptr(res.q_mag), _ptr(res.k_mag), _ptr(q), _ptr(k),
+        _ptr(res.q_lo), _ptr(res.k_lo), _ptr(res.q_hi), _ptr(res.k_hi), _ptr(res.q_mag),
+        _ptr(res.k_mag), _ptr(q), _ptr(k),
         _ptr(wq), _ptr(wk), fmt, T, Hq, Hk, D, rotary_dim, layout, _ptr(positions), _ptr(cos),
         _ptr(sin), cache_len, eps, weight_offset, inv_scale, eta)
     _check(rc, "qk_norm_rope")

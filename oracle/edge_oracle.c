@@ -414,13 +414,16 @@ int oracle_rope(void* out, int out_fmt, const void* x, int f, int64_t tokens, in
 /* Diagnostics of one output element of the QK prologue, for the tests'
  * tie policy (GPU and oracle round in different precisions):
  *   pre  the exact value whose output rounding (or FP8 epilogue) gives out;
- *   alt  the same value when an intermediate rounding went to the other
- *        neighbour at a near tie, else NaN;
+ *   lo, hi  the smallest and largest such value over every combination of
+ *        the intermediate roundings of the element (and of its rotation
+ *        partner) that were decided within the near-tie band: each near-tie
+ *        member may have gone to either neighbour;
  *   mag  the magnitude that sets the error scale: the pair norm for a
  *        rotated channel, |pre| otherwise. */
 typedef struct {
     double* pre;
-    double* alt;
+    double* lo;
+    double* hi;
     double* mag;
 } qk_diag;
 
@@ -440,7 +443,7 @@ static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, const do
                      int64_t t, int heads, int D, int rho, int layout, int rot, int64_t p,
                      const float* cs, const float* sn, float eps, int delta, float inv_scale,
                      double eta, double* xr, double* n, double* m, double* malt, int* tie,
-                     double* y, double* yalt)
+                     double* y, double* ylo, double* yhi)
 {
     int half = rho / 2;
     for (int h = 0; h < heads; ++h) {
@@ -455,7 +458,8 @@ static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, const do
             malt[i] = m[i];
             tie[i] = (f != OR_F32) && near_tie(n[i], f, eta, &malt[i]);
             y[i] = m[i];
-            yalt[i] = malt[i];
+            ylo[i] = fmin(m[i], malt[i]);
+            yhi[i] = fmax(m[i], malt[i]);
         }
         if (rot) {
             for (int j = 0; j < half; ++j) {
@@ -463,7 +467,23 @@ static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, const do
                 pair_index(layout, rho, j, &ia, &ib);
                 double c = (double)cs[p * half + j], s = (double)sn[p * half + j];
                 rotate(m[ia], m[ib], c, s, &y[ia], &y[ib]);
-                rotate(malt[ia], malt[ib], c, s, &yalt[ia], &yalt[ib]);
+                /* bounds over every near-tie neighbour combination of the pair */
+                const double ca[2] = {m[ia], malt[ia]}, cb[2] = {m[ib], malt[ib]};
+                double alo = INFINITY, ahi = -INFINITY, blo = INFINITY, bhi = -INFINITY;
+                for (int u = 0; u < (tie[ia] ? 2 : 1); ++u) {
+                    for (int v = 0; v < (tie[ib] ? 2 : 1); ++v) {
+                        double ra, rb;
+                        rotate(ca[u], cb[v], c, s, &ra, &rb);
+                        alo = fmin(alo, ra);
+                        ahi = fmax(ahi, ra);
+                        blo = fmin(blo, rb);
+                        bhi = fmax(bhi, rb);
+                    }
+                }
+                ylo[ia] = alo;
+                yhi[ia] = ahi;
+                ylo[ib] = blo;
+                yhi[ib] = bhi;
             }
         }
         for (int i = 0; i < D; ++i) {
@@ -474,21 +494,26 @@ static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, const do
                 else partner = i < half ? i + half : i - half;
             }
             store(out, out_fmt, base + i, emit(y[i], out_fmt, inv_scale));
-            double pre, alt = NAN, mag;
+            double pre, lo, hi, mag;
             if (rotated) {
                 pre = y[i];
-                if (tie[i] || tie[partner]) alt = yalt[i];
+                lo = ylo[i];
+                hi = yhi[i];
                 mag = sqrt(y[i] * y[i] + y[partner] * y[partner]);
             } else if (out_fmt == OR_E4M3) {
+                /* the epilogue quantizes the rounded m (or its near-tie neighbour) */
                 pre = m[i];
-                if (tie[i]) alt = malt[i];
+                lo = ylo[i];
+                hi = yhi[i];
                 mag = fabs(pre);
             } else {
-                pre = n[i];
+                /* the output is the rounding of n itself */
+                pre = lo = hi = n[i];
                 mag = fabs(pre);
             }
             if (dg.pre) dg.pre[base + i] = pre;
-            if (dg.alt) dg.alt[base + i] = alt;
+            if (dg.lo) dg.lo[base + i] = lo;
+            if (dg.hi) dg.hi[base + i] = hi;
             if (dg.mag) dg.mag[base + i] = mag;
         }
     }
@@ -504,7 +529,8 @@ static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, const do
  * negative or at least cache_len is normalized but not rotated and reads no
  * cache row.  eta is the relative band of the near-tie diagnostics. */
 int oracle_qk_norm_rope(void* q_out, void* k_out, int out_fmt, double* q_pre, double* k_pre,
-                        double* q_alt, double* k_alt, double* q_mag, double* k_mag,
+                        double* q_lo, double* k_lo, double* q_hi, double* k_hi,
+                        double* q_mag, double* k_mag,
                         const void* q, const void* k, const void* wq, const void* wk, int f,
                         int64_t tokens, int q_heads, int k_heads, int head_dim, int rotary_dim,
                         int layout, const int64_t* positions, const float* cos_cache,
@@ -518,23 +544,25 @@ int oracle_qk_norm_rope(void* q_out, void* k_out, int out_fmt, double* q_pre, do
     size_t nd = (size_t)head_dim + 1;
     double* wqr = malloc(sizeof(double) * nd);
     double* wkr = malloc(sizeof(double) * nd);
-    double* buf = malloc(sizeof(double) * nd * 7);
+    double* buf = malloc(sizeof(double) * nd * 8);
     int* tie = malloc(sizeof(int) * nd);
     if (!wqr || !wkr || !buf || !tie) { free(wqr); free(wkr); free(buf); free(tie); return 2; }
     for (int i = 0; i < head_dim; ++i) {
         wqr[i] = wq ? load(wq, f, i) : 1.0;
         wkr[i] = wk ? load(wk, f, i) : 1.0;
     }
-    qk_diag dq = {q_pre, q_alt, q_mag}, dk = {k_pre, k_alt, k_mag};
+    qk_diag dq = {q_pre, q_lo, q_hi, q_mag}, dk = {k_pre, k_lo, k_hi, k_mag};
     for (int64_t t = 0; t < tokens; ++t) {
         int64_t p = positions ? positions[t] : -1;
         int rot = rotary_dim > 0 && in_cache(p, cache_len);
         qk_heads(q_out, out_fmt, dq, q, wq ? wqr : NULL, f, t, q_heads, head_dim, rotary_dim,
                  layout, rot, p, cos_cache, sin_cache, eps, weight_offset, inv_scale, eta,
-                 buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd);
+                 buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd,
+                 buf + 6 * nd);
         qk_heads(k_out, out_fmt, dk, k, wk ? wkr : NULL, f, t, k_heads, head_dim, rotary_dim,
                  layout, rot, p, cos_cache, sin_cache, eps, weight_offset, inv_scale, eta,
-                 buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd);
+                 buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd,
+                 buf + 6 * nd);
     }
     free(wqr); free(wkr); free(buf); free(tie);
     return 0;

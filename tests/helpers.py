@@ -6,8 +6,8 @@ Acceptance rules (the GPU computes in fp32, the oracle in fp64):
 * bf16/fp16 outputs must lie within 1 ulp of the oracle's rounded value;
 * the strict check additionally requires every output to be a correct
   rounding of some value within ``eta * mag`` of the oracle's exact value
-  ``pre`` (or of its alternate ``alt``, when an intermediate rounding was at
-  a near tie).  That is bit-exactness except near rounding boundaries, with a
+  (or of the interval of values an intermediate rounding at a near tie can
+  lead to).  That is bit-exactness except near rounding boundaries, with a
   band ``eta`` derived from the fp32 error of the kernel;
 * FP8 codes are held to the strict check (bit-exact outside the band);
 * fp32 outputs must satisfy |y - pre| <= rel * mag (+ a tiny absolute floor).
@@ -81,26 +81,16 @@ def _round_codes(v: np.ndarray, out_fmt: int, inv_scale: float) -> np.ndarray:
     return oracle.encode(v, out_fmt)
 
 
-def strict_ok(got: np.ndarray, pre: np.ndarray, mag: np.ndarray, out_fmt: int, eta: float,
-              inv_scale: float = 1.0, alt: np.ndarray | None = None) -> np.ndarray:
-    """Per element: got is the rounding of some value in [pre - eta*mag, pre + eta*mag]
-    (rounding is monotone, so it suffices to bracket the two ends)."""
+def strict_ok(got: np.ndarray, lo: np.ndarray, hi: np.ndarray, mag: np.ndarray, out_fmt: int,
+              eta, inv_scale: float = 1.0) -> np.ndarray:
+    """Per element: got is the rounding of some value in
+    [lo - eta*mag, hi + eta*mag].  lo = hi = the exact value, except where an
+    intermediate rounding sat at a near tie (then [lo, hi] spans the
+    candidates).  Rounding is monotone, so it suffices to bracket the ends."""
     got_o = ordered(got, out_fmt)
-
-    def inside(center):
-        lo = _round_codes(center - eta * mag, out_fmt, inv_scale)
-        hi = _round_codes(center + eta * mag, out_fmt, inv_scale)
-        lo_o, hi_o = ordered(lo, out_fmt), ordered(hi, out_fmt)
-        return (got_o >= np.minimum(lo_o, hi_o)) & (got_o <= np.maximum(lo_o, hi_o))
-
-    ok = inside(pre)
-    if alt is not None:
-        has = ~np.isnan(alt)
-        if has.any():
-            ok_alt = np.zeros_like(ok)
-            ok_alt[has] = inside(np.where(has, alt, 0.0))[has]
-            ok |= ok_alt
-    return ok
+    a = ordered(_round_codes(lo - eta * mag, out_fmt, inv_scale), out_fmt)
+    b = ordered(_round_codes(hi + eta * mag, out_fmt, inv_scale), out_fmt)
+    return (got_o >= np.minimum(a, b)) & (got_o <= np.maximum(a, b))
 
 
 def f32_ok(got: np.ndarray, pre: np.ndarray, mag: np.ndarray, rel: float,

@@ -81,30 +81,32 @@ def calib_inv(pre):
     return float(np.float32(1.0) / np.float32(amax / 448.0))
 
 
-def check_dtype_out(name, got, ref_bits, pre, mag, fmt, eta, alt=None):
+def check_dtype_out(name, got, ref_bits, lo, hi, mag, fmt, eta):
     """bf16/fp16: <= 1 ulp everywhere (at the pair norm for rotated channels)
     and the strict check."""
     one = within_one_ulp(got, ref_bits, mag, fmt)
     assert one.all(), report(name + " (1 ulp)", one)
     d = ulp_distance(got, ref_bits, fmt)
-    ok = strict_ok(got, pre, mag, fmt, eta, alt=alt)
+    ok = strict_ok(got, lo, hi, mag, fmt, eta)
     assert ok.all(), report(name, ok)
     return float(np.mean(d == 0))
 
 
-def check_fp8_out(name, got, pre, mag, eta, inv, alt=None):
-    ok = strict_ok(got, pre, mag, oracle.E4M3, eta, inv_scale=inv, alt=alt)
+def check_fp8_out(name, got, lo, hi, mag, eta, inv):
+    ok = strict_ok(got, lo, hi, mag, oracle.E4M3, eta, inv_scale=inv)
     assert ok.all(), report(name, ok)
 
 
-def check_out(name, got, ref_bits, pre, mag, fmt, out_fmt, eta, inv=1.0, alt=None):
+def check_out(name, got, ref_bits, pre, mag, fmt, out_fmt, eta, inv=1.0, lo=None, hi=None):
+    lo = pre if lo is None else lo
+    hi = pre if hi is None else hi
     if out_fmt == oracle.E4M3:
-        check_fp8_out(name, got, pre, mag, eta, inv, alt)
+        check_fp8_out(name, got, lo, hi, mag, eta, inv)
     elif fmt == oracle.F32:
         ok = f32_ok(got, pre, mag, 2e-6)
         assert ok.all(), report(name, ok)
     else:
-        check_dtype_out(name, got, ref_bits, pre, mag, fmt, eta, alt)
+        check_dtype_out(name, got, ref_bits, lo, hi, mag, fmt, eta)
 
 
 # ---------------------------------------------------------------- QK prologue
@@ -156,6 +158,29 @@ QK_CASES = {
                         w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=16, positions="arange"),
     "no_weight": dict(dtype=torch.bfloat16, T=4, Hq=8, Hk=2, D=256, rot=64, layout=0,
                       w_mean=None, w_std=0.0, offset=0, theta=1e7, P=64, positions="arange"),
+    # many heads (>= 128 per SM): the four-threads-per-head path
+    "quad_f32_d128": dict(dtype=torch.float32, T=2001, Hq=8, Hk=2, D=128, rot=128, layout=0,
+                          w_mean=0.0, w_std=0.1, offset=1, theta=1e6, P=4096,
+                          positions=np.r_[np.arange(1999), [4096, -3]]),
+    "quad_f16_d64_interleaved": dict(dtype=torch.float16, T=2500, Hq=4, Hk=4, D=64, rot=32,
+                                     layout=1, w_mean=0.0, w_std=0.1, offset=1, theta=1e4,
+                                     P=4096, positions="arange"),
+    "quad_bf16_d128_no_k": dict(dtype=torch.bfloat16, T=650, Hq=32, Hk=0, D=128, rot=128,
+                                layout=0, w_mean=1.0, w_std=0.02, offset=0, theta=1e6,
+                                P=4096, positions="offset", inplace=True),
+    "quad_no_weight": dict(dtype=torch.bfloat16, T=700, Hq=24, Hk=4, D=256, rot=64, layout=0,
+                           w_mean=None, w_std=0.0, offset=0, theta=1e7, P=32768,
+                           positions="offset"),
+    "quad_cfg4_interleaved": dict(dtype=torch.bfloat16, T=1000, Hq=16, Hk=8, D=256, rot=256,
+                                  layout=1, w_mean=1.0, w_std=0.02, offset=0, theta=1e6,
+                                  P=4096, positions="arange", inplace=True),
+    "quad_no_rotation": dict(dtype=torch.float16, T=800, Hq=24, Hk=4, D=256, rot=0, layout=0,
+                             w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=16,
+                             positions="arange"),
+    # rotary width whose pairs are not thread-local: the lane-group path serves it
+    "quad_declined_rot32": dict(dtype=torch.bfloat16, T=800, Hq=24, Hk=4, D=256, rot=32,
+                                layout=0, w_mean=0.0, w_std=0.05, offset=1, theta=1e7,
+                                P=32768, positions="offset"),
 }
 
 
@@ -208,19 +233,20 @@ def test_qk_norm_rope(name):
     c = QK_CASES[name]
     ref, gq, gk, fmt, out_fmt, inv = run_qk(c)
     check_out(name + " q", gq, ref.q_out, ref.q_pre, ref.q_mag, fmt, out_fmt, ETA_NORM,
-              alt=ref.q_alt)
+              lo=ref.q_lo, hi=ref.q_hi)
     if c["Hk"]:
         check_out(name + " k", gk, ref.k_out, ref.k_pre, ref.k_mag, fmt, out_fmt, ETA_NORM,
-                  alt=ref.k_alt)
+                  lo=ref.k_lo, hi=ref.k_hi)
 
 
 @pytest.mark.parametrize("name", ["cfg3_16_2_T333", "cfg3_24_4_T8", "cfg4_bf16", "cfg1_f32",
-                                  "generic_odd_d37", "d128_bf16"])
+                                  "generic_odd_d37", "d128_bf16", "quad_f32_d128",
+                                  "quad_f16_d64_interleaved", "quad_cfg4_interleaved"])
 def test_qk_norm_rope_fp8(name):
     c = dict(QK_CASES[name])
     ref, gq, gk, fmt, out_fmt, inv = run_qk(c, fp8=True)
-    check_fp8_out(name + " q", gq, ref.q_pre, ref.q_mag, ETA_NORM, inv, alt=ref.q_alt)
-    check_fp8_out(name + " k", gk, ref.k_pre, ref.k_mag, ETA_NORM, inv, alt=ref.k_alt)
+    check_fp8_out(name + " q", gq, ref.q_lo, ref.q_hi, ref.q_mag, ETA_NORM, inv)
+    check_fp8_out(name + " k", gk, ref.k_lo, ref.k_hi, ref.k_mag, ETA_NORM, inv)
 
 
 @pytest.mark.parametrize("geom", [(16, 2), (24, 4)])
@@ -229,8 +255,10 @@ def test_qk_text_profile_full_size(geom, T):
     # workload 3 at its sweep sizes, in the launch configuration the benchmark times
     c = dict(QK_CASES["cfg3_16_2_T1"], T=T, Hq=geom[0], Hk=geom[1])
     ref, gq, gk, fmt, out_fmt, _ = run_qk(c)
-    check_out("q", gq, ref.q_out, ref.q_pre, ref.q_mag, fmt, out_fmt, ETA_NORM, alt=ref.q_alt)
-    check_out("k", gk, ref.k_out, ref.k_pre, ref.k_mag, fmt, out_fmt, ETA_NORM, alt=ref.k_alt)
+    check_out("q", gq, ref.q_out, ref.q_pre, ref.q_mag, fmt, out_fmt, ETA_NORM, lo=ref.q_lo,
+              hi=ref.q_hi)
+    check_out("k", gk, ref.k_out, ref.k_pre, ref.k_mag, fmt, out_fmt, ETA_NORM, lo=ref.k_lo,
+              hi=ref.k_hi)
 
 
 def test_qk_out_of_cache_token_untouched_by_rotation():

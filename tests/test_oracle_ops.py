@@ -401,3 +401,16 @@ def test_fp8_qk_quantizes_rotated_and_rounded_values():
     assert np.array_equal(r8.q_out[:, :, 64:], oracle.quantize(m[:, :, 64:], 32.0))
     assert np.array_equal(r8.q_out[2], oracle.quantize(m[2], 32.0))
     assert np.array_equal(r8.q_out, oracle.quantize(r8.q_pre, 32.0))
+
+
+def test_tie_bounds_bracket_the_exact_value():
+    # diagnostics for the GPU tie policy: lo <= pre <= hi everywhere, and the
+    # interval is non-trivial only where an intermediate rounding was near a tie
+    inp, r = _qk(torch.float16, T=64, Hq=8, Hk=2, D=64, rho=32, layout=oracle.INTERLEAVED,
+                 positions="arange", cache_len=128)
+    for lo, pre, hi in ((r.q_lo, r.q_pre, r.q_hi), (r.k_lo, r.k_pre, r.k_hi)):
+        assert np.all(lo <= pre) and np.all(pre <= hi)
+    wide = np.count_nonzero(r.q_hi > r.q_lo) + np.count_nonzero(r.k_hi > r.k_lo)
+    assert 0 < wide < 0.2 * (r.q_lo.size + r.k_lo.size)
+    # pass-through channels of a bf16/fp16 output round n itself: no interval
+    assert np.array_equal(r.q_lo[..., 32:], r.q_hi[..., 32:])

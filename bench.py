@@ -277,7 +277,12 @@ class Layer:
 
 
 def build_layers(torch, synth, device, seed):
-    """Per-layer device buffers; values from one seeded layer, copied into each."""
+    """Per-layer device buffers, carved from three arenas so that the
+    end-to-end leg moves each direction in two large copies:
+      A (in and out): residual, q, k of every layer;
+      B (in only):    mlp_out, attn_out, gate_up;
+      C (out only):   h1, h2, act.
+    Values come from one seeded layer, copied into every layer."""
     bf = torch.bfloat16
     r1 = synth.rows_inputs(seed, bf, T_DEC, HID)
     r2 = synth.rows_inputs(seed + 100, bf, T_DEC, HID)
@@ -286,23 +291,39 @@ def build_layers(torch, synth, device, seed):
     g = synth.glu_inputs(seed, bf, T_DEC, INTER)
     shared = dict(pos=q["positions"].to(device), cos=q["cos"].to(device),
                   sin=q["sin"].to(device))
+    n_res, n_q, n_k = T_DEC * HID, T_DEC * HQ * HD, T_DEC * HK * HD
+    n_gu, n_act = T_DEC * 2 * INTER, T_DEC * INTER
+    per_a = n_res + n_q + n_k
+    per_b = 2 * n_res + n_gu
+    per_c = 2 * n_res + n_act
+    A = torch.empty(LAYERS * per_a, dtype=bf, device=device)
+    B = torch.empty(LAYERS * per_b, dtype=bf, device=device)
+    C = torch.empty(LAYERS * per_c, dtype=bf, device=device)
     layers = []
-    for _ in range(LAYERS):
+    for i in range(LAYERS):
         L = Layer()
-        L.mlp_out = r1["x"].to(device)
-        L.res = r1["residual"].to(device)
+        a, b, c = A[i * per_a:(i + 1) * per_a], B[i * per_b:(i + 1) * per_b], C[i * per_c:(i + 1) * per_c]
+        L.res = a[:n_res].view(T_DEC, HID)
+        L.q = a[n_res:n_res + n_q].view(T_DEC, HQ, HD)
+        L.k = a[n_res + n_q:].view(T_DEC, HK, HD)
+        L.mlp_out = b[:n_res].view(T_DEC, HID)
+        L.attn_out = b[n_res:2 * n_res].view(T_DEC, HID)
+        L.gate_up = b[2 * n_res:].view(T_DEC, 2 * INTER)
+        L.h1 = c[:n_res].view(T_DEC, HID)
+        L.h2 = c[n_res:2 * n_res].view(T_DEC, HID)
+        L.act = c[2 * n_res:].view(T_DEC, INTER)
+        L.res.copy_(r1["residual"])
+        L.q.copy_(q["q"])
+        L.k.copy_(q["k"])
+        L.mlp_out.copy_(r1["x"])
+        L.attn_out.copy_(r2["x"])
+        L.gate_up.copy_(g["gate_up"])
         L.w_in = r1["w"].to(device)
-        L.h1 = torch.empty_like(L.mlp_out)
-        L.q = q["q"].to(device)
-        L.k = q["k"].to(device)
+        L.w_post = r2["w"].to(device)
         L.wq = q["wq"].to(device)
         L.wk = q["wk"].to(device)
-        L.attn_out = r2["x"].to(device)
-        L.w_post = r2["w"].to(device)
-        L.h2 = torch.empty_like(L.attn_out)
-        L.gate_up = g["gate_up"].to(device)
-        L.act = torch.empty(T_DEC, INTER, dtype=bf, device=device)
         layers.append(L)
+    shared["arenas"] = (A, B, C)
     return layers, shared
 
 
@@ -616,22 +637,22 @@ def main():
         sampler.stop()
 
     # ---- e2e: pinned host inputs -> device, the step, results -> host
-    h2d_pairs, d2h_pairs = [], []
-    for L in layers:
-        for t in (L.mlp_out, L.res, L.q, L.k, L.attn_out, L.gate_up):
-            h2d_pairs.append((torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t), t))
-        for t in (L.res, L.h1, L.q, L.k, L.h2, L.act):
-            d2h_pairs.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
-    h2d_bytes = sum(d.numel() * d.element_size() for _, d in h2d_pairs)
-    d2h_bytes = sum(d.numel() * d.element_size() for d, _ in d2h_pairs)
+    # (the activations live in arenas: two copies in, two copies out)
+    A, B, C = sh["arenas"]
+    hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True).copy_(A)
+    hB = torch.empty(B.shape, dtype=B.dtype, pin_memory=True).copy_(B)
+    oA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True)
+    oC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+    h2d_bytes = (A.numel() + B.numel()) * A.element_size()
+    d2h_bytes = (A.numel() + C.numel()) * A.element_size()
     e2e_steps = max(1, min(args.steps, 50))
 
     def e2e_step():
-        for h, d in h2d_pairs:
-            d.copy_(h, non_blocking=True)
+        A.copy_(hA, non_blocking=True)
+        B.copy_(hB, non_blocking=True)
         graph.replay()
-        for d, h in d2h_pairs:
-            h.copy_(d, non_blocking=True)
+        oA.copy_(A, non_blocking=True)
+        oC.copy_(C, non_blocking=True)
 
     with torch.cuda.stream(stream):
         e2e_step()

@@ -177,6 +177,42 @@ edge_status edge_qk_norm_rope(void* q_out, void* k_out, edge_dtype out_dt, const
                               int64_t cache_len, float eps, int weight_offset, float inv_scale,
                               void* stream);
 
+/* Flags of edge_qk_norm_rope_ex. */
+enum {
+    /* Rotate the fp32 normalized value and round once after the rotation,
+     * instead of rotating its rounding to dt.  This is the variant the
+     * ninfer review asks for (item 1).  Channels that do not rotate are
+     * unchanged (they carry round_dt of the normalized value either way). */
+    EDGE_QK_ROTATE_UNROUNDED = 1
+};
+
+/*
+ * edge_qk_norm_rope with option flags (EDGE_QK_* above; 0 gives exactly
+ * edge_qk_norm_rope).  Unknown flags return EDGE_ERR_VALUE.
+ */
+edge_status edge_qk_norm_rope_ex(void* q_out, void* k_out, edge_dtype out_dt, const void* q,
+                                 const void* k, const void* wq, const void* wk, edge_dtype dt,
+                                 int64_t tokens, int32_t q_heads, int32_t k_heads,
+                                 int32_t head_dim, int32_t rotary_dim, edge_rope_layout layout,
+                                 const int64_t* positions, const float* cos, const float* sin,
+                                 int64_t cache_len, float eps, int weight_offset, float inv_scale,
+                                 uint32_t flags, void* stream);
+
+/*
+ * Standalone rotary embedding ("thox-edge-ops v2", section 5.1, the rotary
+ * operator: query and key in one launch).  For every head of q and k of token
+ * t with 0 <= positions[t] < cache_len, pair j < rotary_dim/2 (rotate-half or
+ * interleaved, as in edge_qk_norm_rope) becomes a' = a c - b s, b' = b c + a s
+ * in fp32, rounded once (or the FP8 epilogue).  Other channels, and every
+ * channel of a token outside the cache, are copied unchanged.  Same layout,
+ * aliasing and error rules as edge_qk_norm_rope, with no weights and no eps.
+ */
+edge_status edge_rope(void* q_out, void* k_out, edge_dtype out_dt, const void* q, const void* k,
+                      edge_dtype dt, int64_t tokens, int32_t q_heads, int32_t k_heads,
+                      int32_t head_dim, int32_t rotary_dim, edge_rope_layout layout,
+                      const int64_t* positions, const float* cos, const float* sin,
+                      int64_t cache_len, float inv_scale, void* stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char* edge_status_str(edge_status status);
 

@@ -176,58 +176,14 @@ edge_status rows_entry(void* out, edge_dtype out_dt, const void* x, void* residu
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-edge_status edge_rmsnorm(void* out, edge_dtype out_dt, const void* x, const void* w, edge_dtype dt,
-                         int64_t rows, int64_t hidden, float eps, int weight_offset,
-                         float inv_scale, void* stream) {
-    return rows_entry(out, out_dt, x, nullptr, false, w, dt, rows, hidden, eps, weight_offset,
-                      inv_scale, stream);
-}
-
-edge_status edge_add_rmsnorm(void* out, edge_dtype out_dt, const void* x, void* residual,
-                             const void* w, edge_dtype dt, int64_t rows, int64_t hidden, float eps,
-                             int weight_offset, float inv_scale, void* stream) {
-    return rows_entry(out, out_dt, x, residual, true, w, dt, rows, hidden, eps, weight_offset,
-                      inv_scale, stream);
-}
-
-edge_status edge_glu_act(void* out, edge_dtype out_dt, const void* gate_up, edge_dtype dt,
-                         int64_t rows, int64_t d, edge_act act, float inv_scale, void* stream) {
-    edge_status st = check_out_dt(out_dt, dt);
-    if (st != EDGE_OK) return st;
-    if (out == nullptr || gate_up == nullptr) return EDGE_ERR_NULL;
-    if (rows < 0 || d <= 0) return EDGE_ERR_SHAPE;
-    if (act != EDGE_ACT_SILU && act != EDGE_ACT_GELU_TANH) return EDGE_ERR_VALUE;
-    if ((st = check_scale(out_dt, inv_scale)) != EDGE_OK) return st;
-    int64_t in_bytes = 0, out_bytes = 0;
-    if (d > INT64_MAX / 2 || !checked_bytes(rows, 2 * d, esize(dt), &in_bytes) ||
-        !checked_bytes(rows, d, esize(out_dt), &out_bytes)) {
-        return EDGE_ERR_SHAPE;
-    }
-    if (!aligned(gate_up, esize(dt)) || !aligned(out, esize(out_dt))) return EDGE_ERR_ALIGN;
-    if (overlap(span(out, out_bytes), span(gate_up, in_bytes))) return EDGE_ERR_ALIAS;
-    if (rows == 0) return EDGE_OK;
-
-    edge::GluArgs a;
-    a.gate_up = gate_up;
-    a.out = out;
-    a.rows = rows;
-    a.d = d;
-    a.dt = (int)dt;
-    a.out_dt = (int)out_dt;
-    a.act = (int)act;
-    a.inv_scale = inv_scale;
-    return finish(edge::launch_glu(a, static_cast<cudaStream_t>(stream)));
-}
-
-edge_status edge_qk_norm_rope(void* q_out, void* k_out, edge_dtype out_dt, const void* q,
-                              const void* k, const void* wq, const void* wk, edge_dtype dt,
-                              int64_t tokens, int32_t q_heads, int32_t k_heads, int32_t head_dim,
-                              int32_t rotary_dim, edge_rope_layout layout,
-                              const int64_t* positions, const float* cos, const float* sin,
-                              int64_t cache_len, float eps, int weight_offset, float inv_scale,
-                              void* stream) {
+static edge_status qk_entry(void* q_out, void* k_out, edge_dtype out_dt, const void* q,
+                            const void* k, const void* wq, const void* wk, edge_dtype dt,
+                            int64_t tokens, int32_t q_heads, int32_t k_heads, int32_t head_dim,
+                            int32_t rotary_dim, edge_rope_layout layout, const int64_t* positions,
+                            const float* cos, const float* sin, int64_t cache_len, float eps,
+                            int weight_offset, float inv_scale, int mode, void* stream) {
     edge_status st = check_out_dt(out_dt, dt);
     if (st != EDGE_OK) return st;
     if (q == nullptr || q_out == nullptr) return EDGE_ERR_NULL;
@@ -296,7 +252,91 @@ edge_status edge_qk_norm_rope(void* q_out, void* k_out, edge_dtype out_dt, const
     a.eps = eps;
     a.inv_scale = inv_scale;
     a.weight_offset = weight_offset;
+    a.mode = mode;
     return finish(edge::launch_qk(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+edge_status edge_rmsnorm(void* out, edge_dtype out_dt, const void* x, const void* w, edge_dtype dt,
+                         int64_t rows, int64_t hidden, float eps, int weight_offset,
+                         float inv_scale, void* stream) {
+    return rows_entry(out, out_dt, x, nullptr, false, w, dt, rows, hidden, eps, weight_offset,
+                      inv_scale, stream);
+}
+
+edge_status edge_add_rmsnorm(void* out, edge_dtype out_dt, const void* x, void* residual,
+                             const void* w, edge_dtype dt, int64_t rows, int64_t hidden, float eps,
+                             int weight_offset, float inv_scale, void* stream) {
+    return rows_entry(out, out_dt, x, residual, true, w, dt, rows, hidden, eps, weight_offset,
+                      inv_scale, stream);
+}
+
+edge_status edge_glu_act(void* out, edge_dtype out_dt, const void* gate_up, edge_dtype dt,
+                         int64_t rows, int64_t d, edge_act act, float inv_scale, void* stream) {
+    edge_status st = check_out_dt(out_dt, dt);
+    if (st != EDGE_OK) return st;
+    if (out == nullptr || gate_up == nullptr) return EDGE_ERR_NULL;
+    if (rows < 0 || d <= 0) return EDGE_ERR_SHAPE;
+    if (act != EDGE_ACT_SILU && act != EDGE_ACT_GELU_TANH) return EDGE_ERR_VALUE;
+    if ((st = check_scale(out_dt, inv_scale)) != EDGE_OK) return st;
+    int64_t in_bytes = 0, out_bytes = 0;
+    if (d > INT64_MAX / 2 || !checked_bytes(rows, 2 * d, esize(dt), &in_bytes) ||
+        !checked_bytes(rows, d, esize(out_dt), &out_bytes)) {
+        return EDGE_ERR_SHAPE;
+    }
+    if (!aligned(gate_up, esize(dt)) || !aligned(out, esize(out_dt))) return EDGE_ERR_ALIGN;
+    if (overlap(span(out, out_bytes), span(gate_up, in_bytes))) return EDGE_ERR_ALIAS;
+    if (rows == 0) return EDGE_OK;
+
+    edge::GluArgs a;
+    a.gate_up = gate_up;
+    a.out = out;
+    a.rows = rows;
+    a.d = d;
+    a.dt = (int)dt;
+    a.out_dt = (int)out_dt;
+    a.act = (int)act;
+    a.inv_scale = inv_scale;
+    return finish(edge::launch_glu(a, static_cast<cudaStream_t>(stream)));
+}
+
+edge_status edge_qk_norm_rope(void* q_out, void* k_out, edge_dtype out_dt, const void* q,
+                              const void* k, const void* wq, const void* wk, edge_dtype dt,
+                              int64_t tokens, int32_t q_heads, int32_t k_heads, int32_t head_dim,
+                              int32_t rotary_dim, edge_rope_layout layout,
+                              const int64_t* positions, const float* cos, const float* sin,
+                              int64_t cache_len, float eps, int weight_offset, float inv_scale,
+                              void* stream) {
+    return qk_entry(q_out, k_out, out_dt, q, k, wq, wk, dt, tokens, q_heads, k_heads, head_dim,
+                    rotary_dim, layout, positions, cos, sin, cache_len, eps, weight_offset,
+                    inv_scale, 1 /* normalize */, stream);
+}
+
+edge_status edge_qk_norm_rope_ex(void* q_out, void* k_out, edge_dtype out_dt, const void* q,
+                                 const void* k, const void* wq, const void* wk, edge_dtype dt,
+                                 int64_t tokens, int32_t q_heads, int32_t k_heads,
+                                 int32_t head_dim, int32_t rotary_dim, edge_rope_layout layout,
+                                 const int64_t* positions, const float* cos, const float* sin,
+                                 int64_t cache_len, float eps, int weight_offset, float inv_scale,
+                                 uint32_t flags, void* stream) {
+    if ((flags & ~(uint32_t)EDGE_QK_ROTATE_UNROUNDED) != 0) return EDGE_ERR_VALUE;
+    const int mode = 1 | ((flags & EDGE_QK_ROTATE_UNROUNDED) ? 2 : 0);
+    return qk_entry(q_out, k_out, out_dt, q, k, wq, wk, dt, tokens, q_heads, k_heads, head_dim,
+                    rotary_dim, layout, positions, cos, sin, cache_len, eps, weight_offset,
+                    inv_scale, mode, stream);
+}
+
+edge_status edge_rope(void* q_out, void* k_out, edge_dtype out_dt, const void* q, const void* k,
+                      edge_dtype dt, int64_t tokens, int32_t q_heads, int32_t k_heads,
+                      int32_t head_dim, int32_t rotary_dim, edge_rope_layout layout,
+                      const int64_t* positions, const float* cos, const float* sin,
+                      int64_t cache_len, float inv_scale, void* stream) {
+    return qk_entry(q_out, k_out, out_dt, q, k, nullptr, nullptr, dt, tokens, q_heads, k_heads,
+                    head_dim, rotary_dim, layout, positions, cos, sin, cache_len, 0.0f, 0,
+                    inv_scale, 0 /* rotate only */, stream);
 }
 
 const char* edge_status_str(edge_status status) {

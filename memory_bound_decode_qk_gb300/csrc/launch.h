@@ -26,6 +26,7 @@ struct QKArgs {
     int dt, out_dt;
     float eps, inv_scale;
     int weight_offset;
+    int mode;                // kModeNorm (1) | kModeUnrounded (2), qk_common.cuh
 };
 
 struct RowsArgs {

@@ -10,6 +10,13 @@ namespace edge {
 constexpr int kRotateHalf = 0;
 constexpr int kInterleaved = 1;
 
+// Prologue modes (QKArgs::mode): kModeNorm normalizes each head first (the
+// fused prologue; without it the op is the standalone rotary embedding);
+// kModeUnrounded rotates the fp32 normalized value instead of its rounding to
+// the dtype (the variant asked for in the ninfer review, item 1).
+constexpr int kModeNorm = 1;
+constexpr int kModeUnrounded = 2;
+
 // Kernel parameters of the prologue (validated by the C ABI layer).
 struct QKP {
     const char* q;
@@ -30,6 +37,7 @@ struct QKP {
     int q_heads, k_heads, D, rot, half;
     int in_bytes, out_bytes;  // element sizes of input and output
     float eps, delta, inv, invD;  // invD = 1 / head_dim (fp32)
+    int mode;                     // kModeNorm | kModeUnrounded
 };
 
 struct Unit {

@@ -94,16 +94,29 @@ __device__ __forceinline__ void qk_core(const QKP& p, char* dst, bool active, in
     constexpr int N = vec_elems<T>();
     float x[N];
     unpack_vec<T, N>(raw, x);
-    float ss = 0.0f;
+    // normalized value n (fp32); without normalization n = x
+    float n[N];
+    if (p.mode & kModeNorm) {
+        float ss = 0.0f;
 #pragma unroll
-    for (int i = 0; i < N; ++i) ss = __fmaf_rn(x[i], x[i], ss);
-    ss = group_sum<LPH>(ss);
-    const float r = inv_rms(ss, p.invD, p.eps);
-
-    // normalized value, rounded to the activation dtype before the rotation
-    float m[N];
+        for (int i = 0; i < N; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+        ss = group_sum<LPH>(ss);
+        const float r = inv_rms(ss, p.invD, p.eps);
 #pragma unroll
-    for (int i = 0; i < N; ++i) m[i] = round_to<T>(__fmul_rn(__fmul_rn(x[i], r), w[i]));
+        for (int i = 0; i < N; ++i) n[i] = __fmul_rn(__fmul_rn(x[i], r), w[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) n[i] = x[i];
+    }
+    // m: n rounded to the activation dtype.  The rotation consumes m, or n
+    // itself in the unrounded mode; channels that do not rotate emit m.
+    const bool unrounded = (p.mode & kModeUnrounded) != 0;
+    float m[N], src[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        m[i] = round_to<T>(n[i]);
+        src[i] = unrounded ? n[i] : m[i];
+    }
 
     float y[N];
 #pragma unroll
@@ -113,7 +126,7 @@ __device__ __forceinline__ void qk_core(const QKP& p, char* dst, bool active, in
         if (role != 0) {
 #pragma unroll
             for (int i = 0; i < N / 2; ++i) {
-                const float a = m[2 * i], b = m[2 * i + 1];
+                const float a = src[2 * i], b = src[2 * i + 1];
                 y[2 * i] = __fmaf_rn(a, cr.c[i], -__fmul_rn(b, cr.s[i]));
                 y[2 * i + 1] = __fmaf_rn(b, cr.c[i], __fmul_rn(a, cr.s[i]));
             }
@@ -122,23 +135,26 @@ __device__ __forceinline__ void qk_core(const QKP& p, char* dst, bool active, in
         // rotate-half: channel e pairs with e + half; the partner vector is
         // held by the lane half/N positions away in the same lane group
         const int hv = p.half / N;
-        const int src = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
-        const uint4 mine = pack_vec<T, N>(m);  // exact: m is already rounded to T
-        uint4 other;
-        other.x = __shfl_sync(0xffffffffu, mine.x, src);
-        other.y = __shfl_sync(0xffffffffu, mine.y, src);
-        other.z = __shfl_sync(0xffffffffu, mine.z, src);
-        other.w = __shfl_sync(0xffffffffu, mine.w, src);
-        if (role != 0) {
-            float pm[N];
+        const int from = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
+        float pm[N];
+        if (unrounded) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) pm[i] = __shfl_sync(0xffffffffu, src[i], from);
+        } else {
+            const uint4 mine = pack_vec<T, N>(m);  // exact: m is already rounded to T
+            uint4 other;
+            other.x = __shfl_sync(0xffffffffu, mine.x, from);
+            other.y = __shfl_sync(0xffffffffu, mine.y, from);
+            other.z = __shfl_sync(0xffffffffu, mine.z, from);
+            other.w = __shfl_sync(0xffffffffu, mine.w, from);
             unpack_vec<T, N>(other, pm);
-            if (role == 1) {
+        }
+        if (role == 1) {
 #pragma unroll
-                for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(m[i], cr.c[i], -__fmul_rn(pm[i], cr.s[i]));
-            } else {
+            for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(src[i], cr.c[i], -__fmul_rn(pm[i], cr.s[i]));
+        } else if (role == 2) {
 #pragma unroll
-                for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(m[i], cr.c[i], __fmul_rn(pm[i], cr.s[i]));
-            }
+            for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(src[i], cr.c[i], __fmul_rn(pm[i], cr.s[i]));
         }
     }
 
@@ -231,18 +247,25 @@ __global__ void __launch_bounds__(128) qk_generic_kernel(QKP p, int layout) {
             hm[e] = v;
             ss = __fmaf_rn(v, v, ss);
         }
-        ss = group_sum<32>(ss);
-        const float r = inv_rms(ss, p.invD, p.eps);
-        for (int e = lane; e < p.D; e += 32) {
-            float w = un.w ? __fadd_rn(ld_elem<T>(un.w, e), p.delta) : 1.0f;
-            hm[e] = round_to<T>(__fmul_rn(__fmul_rn(hm[e], r), w));
+        const bool norm = (p.mode & kModeNorm) != 0;
+        const bool unrounded = (p.mode & kModeUnrounded) != 0;
+        if (norm) {
+            ss = group_sum<32>(ss);
+            const float r = inv_rms(ss, p.invD, p.eps);
+            // the staged value is what the rotation consumes: the normalized
+            // value, rounded to the dtype unless in the unrounded mode
+            for (int e = lane; e < p.D; e += 32) {
+                float w = un.w ? __fadd_rn(ld_elem<T>(un.w, e), p.delta) : 1.0f;
+                const float n = __fmul_rn(__fmul_rn(hm[e], r), w);
+                hm[e] = unrounded ? n : round_to<T>(n);
+            }
         }
         __syncwarp();
         int64_t pos = -1;
         if (p.rot > 0) pos = p.pos[un.t];
         const bool rot = pos >= 0 && pos < p.cache_len;
         for (int e = lane; e < p.D; e += 32) {
-            float y = hm[e];
+            float y = round_to<T>(hm[e]);
             if (rot && e < p.rot) {
                 int j, partner;
                 bool first;
@@ -257,9 +280,9 @@ __global__ void __launch_bounds__(128) qk_generic_kernel(QKP p, int layout) {
                 }
                 const float c = p.cs[pos * p.half + j];
                 const float sn = p.sn[pos * p.half + j];
-                const float other = hm[partner];
-                y = first ? __fmaf_rn(y, c, -__fmul_rn(other, sn))
-                          : __fmaf_rn(y, c, __fmul_rn(other, sn));
+                const float own = hm[e], other = hm[partner];
+                y = first ? __fmaf_rn(own, c, -__fmul_rn(other, sn))
+                          : __fmaf_rn(own, c, __fmul_rn(other, sn));
             }
             if constexpr (FP8) {
                 reinterpret_cast<uint8_t*>(un.dst)[e] = quantize1(y, p.inv);
@@ -394,6 +417,7 @@ cudaError_t launch_qk(const QKArgs& args, cudaStream_t s) {
     p.delta = (float)a.weight_offset;
     p.inv = a.inv_scale;
     p.invD = 1.0f / (float)a.head_dim;
+    p.mode = a.mode;
     const bool fp8 = a.out_dt == kFP8;
     switch (a.dt) {
         case kF32:

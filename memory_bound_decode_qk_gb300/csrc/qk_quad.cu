@@ -39,7 +39,7 @@ constexpr int K = 4;  // threads per head
 // RQ: rotate-half: chunks per thread that are first members (HVQ); interleaved:
 // chunks per thread that rotate.  0: no channel rotates.
 template <typename T, bool FP8, int C, int LAYOUT, int RQ>
-__global__ void __launch_bounds__(256) qk_quad_kernel(QKP p) {
+__global__ void __launch_bounds__(256, FP8 ? 2 : 3) qk_quad_kernel(QKP p) {
     constexpr int N = vec_elems<T>();
     constexpr int D = C * K * N;
     static_assert(LAYOUT == kInterleaved ? RQ <= C : 2 * RQ <= C, "rotated chunks exceed the head");
@@ -91,7 +91,8 @@ __global__ void __launch_bounds__(256) qk_quad_kernel(QKP p) {
         }
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        const float r = inv_rms(ss, p.invD, p.eps);
+        // without normalization (standalone rotary) r = 1 and w = 1: m = x
+        const float r = (p.mode & kModeNorm) ? inv_rms(ss, p.invD, p.eps) : 1.0f;
 
         // normalized value rounded to the dtype, packed (exactly) over the
         // loaded vectors, which are no longer needed
@@ -169,9 +170,10 @@ __global__ void __launch_bounds__(256) qk_quad_kernel(QKP p) {
 #pragma unroll
             for (int i = 0; i < C; ++i) {
                 if (i < RQ && rot) {
-                    // chunk i (first members) with chunk i + RQ (their partners)
+                    // chunk i (first members) with chunk i + RQ (their partners),
+                    // four channels at a time to keep few values live
                     const int c = kt + K * i;
-                    float a[N], b[N], ya[N], yb[N], cs[N], sn[N];
+                    float a[N], b[N];
                     unpack_vec<T, N>(mp[i], a);
                     unpack_vec<T, N>(mp[i + RQ], b);
                     const float4* c4 = reinterpret_cast<const float4*>(p.cs + pos * p.half + c * N);
@@ -179,16 +181,17 @@ __global__ void __launch_bounds__(256) qk_quad_kernel(QKP p) {
 #pragma unroll
                     for (int v = 0; v < N / 4; ++v) {
                         const float4 cc = __ldg(c4 + v), sv = __ldg(s4 + v);
-                        cs[4 * v] = cc.x; cs[4 * v + 1] = cc.y; cs[4 * v + 2] = cc.z; cs[4 * v + 3] = cc.w;
-                        sn[4 * v] = sv.x; sn[4 * v + 1] = sv.y; sn[4 * v + 2] = sv.z; sn[4 * v + 3] = sv.w;
-                    }
+                        const float cs[4] = {cc.x, cc.y, cc.z, cc.w};
+                        const float sn[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-                    for (int e = 0; e < N; ++e) {
-                        ya[e] = __fmaf_rn(a[e], cs[e], -__fmul_rn(b[e], sn[e]));
-                        yb[e] = __fmaf_rn(b[e], cs[e], __fmul_rn(a[e], sn[e]));
+                        for (int e = 0; e < 4; ++e) {
+                            const float ae = a[4 * v + e], be = b[4 * v + e];
+                            a[4 * v + e] = __fmaf_rn(ae, cs[e], -__fmul_rn(be, sn[e]));
+                            b[4 * v + e] = __fmaf_rn(be, cs[e], __fmul_rn(ae, sn[e]));
+                        }
                     }
-                    emit(i, ya);
-                    emit(i + RQ, yb);
+                    emit(i, a);
+                    emit(i + RQ, b);
                 } else if (i < RQ || i >= 2 * RQ || !rot) {
                     emit_m(i);
                 }
@@ -228,6 +231,7 @@ template <typename T, bool FP8>
 cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg, bool* handled) {
     constexpr int N = vec_elems<T>();
     *handled = false;
+    if (a.mode & kModeUnrounded) return cudaSuccess;  // served by the lane-group path
     const int64_t hb = (int64_t)a.head_dim * (int64_t)sizeof(T);
     if (hb % (16 * K) != 0) return cudaSuccess;
     const int C = (int)(hb / (16 * K));

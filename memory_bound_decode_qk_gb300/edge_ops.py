@@ -25,7 +25,9 @@ STATUS = {
     8: "EDGE_ERR_VALUE",
 }
 EXPORTS = ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope",
-           "edge_status_str", "edge_last_cuda_error", "edge_version")
+           "edge_qk_norm_rope_ex", "edge_rope", "edge_status_str", "edge_last_cuda_error",
+           "edge_version")
+QK_ROTATE_UNROUNDED = 1
 
 _DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 _LIB = None
@@ -65,7 +67,11 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
     L.edge_glu_act.argtypes = [P, I, P, I, I64, I64, I, F, P]
     L.edge_qk_norm_rope.argtypes = [P, P, I, P, P, P, P, I, I64, I32, I32, I32, I32, I, P, P, P,
                                     I64, F, I, F, P]
-    for name in ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope"):
+    L.edge_qk_norm_rope_ex.argtypes = [P, P, I, P, P, P, P, I, I64, I32, I32, I32, I32, I, P, P,
+                                       P, I64, F, I, F, ctypes.c_uint32, P]
+    L.edge_rope.argtypes = [P, P, I, P, P, I, I64, I32, I32, I32, I32, I, P, P, P, I64, F, P]
+    for name in ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope",
+                 "edge_qk_norm_rope_ex", "edge_rope"):
         getattr(L, name).restype = I
     L.edge_status_str.argtypes = [I]
     L.edge_status_str.restype = ctypes.c_char_p
@@ -156,15 +162,9 @@ def glu_act(gate_up, act=SILU, *, out=None, fp8=False, inv_scale=1.0, stream=Non
     return out
 
 
-def qk_norm_rope(q, k, wq, wk, positions, cos, sin, *, rotary_dim=None, layout=ROTATE_HALF,
-                 eps=1e-6, weight_offset=0, q_out=None, k_out=None, fp8=False, inv_scale=1.0,
-                 cache_len=None, stream=None):
-    """Per-head QK-RMSNorm + RoPE.  q: [T, Hq, D], k: [T, Hk, D];
-    cos/sin: [P, rotary_dim/2] fp32; positions: [T] int64.  Pass q_out=q and
-    k_out=k for the in-place form.  Returns (q_out, k_out)."""
-    _need_contig(q, k, wq, wk, positions, cos, sin, q_out, k_out)
+def _qk_shapes(q, k, cos, rotary_dim, cache_len, layout, fp8, q_out, k_out):
     T, Hq, D = q.shape
-    Hk = k.shape[1]
+    Hk = k.shape[1] if k is not None else 0
     if rotary_dim is None:
         rotary_dim = D if cos is None else 2 * cos.shape[-1]
     if cache_len is None:
@@ -173,12 +173,43 @@ def qk_norm_rope(q, k, wq, wk, positions, cos, sin, *, rotary_dim=None, layout=R
         layout = {"rotate_half": ROTATE_HALF, "interleaved": INTERLEAVED}[layout]
     if q_out is None:
         q_out = _alloc(q, q.shape, fp8)
-    if k_out is None:
+    if k_out is None and k is not None:
         k_out = _alloc(k, k.shape, fp8)
+    return T, Hq, Hk, D, rotary_dim, cache_len, layout, q_out, k_out
+
+
+def qk_norm_rope(q, k, wq, wk, positions, cos, sin, *, rotary_dim=None, layout=ROTATE_HALF,
+                 eps=1e-6, weight_offset=0, q_out=None, k_out=None, fp8=False, inv_scale=1.0,
+                 cache_len=None, unrounded=False, stream=None):
+    """Per-head QK-RMSNorm + RoPE.  q: [T, Hq, D], k: [T, Hk, D];
+    cos/sin: [P, rotary_dim/2] fp32; positions: [T] int64.  Pass q_out=q and
+    k_out=k for the in-place form.  unrounded=True rotates the fp32 normalized
+    value (edge_qk_norm_rope_ex with EDGE_QK_ROTATE_UNROUNDED).  Returns
+    (q_out, k_out)."""
+    _need_contig(q, k, wq, wk, positions, cos, sin, q_out, k_out)
+    T, Hq, Hk, D, rotary_dim, cache_len, layout, q_out, k_out = _qk_shapes(
+        q, k, cos, rotary_dim, cache_len, layout, fp8, q_out, k_out)
     dt = _dt(q)
-    _check(lib().edge_qk_norm_rope(_ptr(q_out), _ptr(k_out), _out_dt(fp8, dt), _ptr(q), _ptr(k),
-                                   _ptr(wq), _ptr(wk), dt, T, Hq, Hk, D, rotary_dim, layout,
-                                   _ptr(positions), _ptr(cos), _ptr(sin), cache_len, eps,
-                                   weight_offset, inv_scale, _stream(stream)),
-           "edge_qk_norm_rope")
+    args = (_ptr(q_out), _ptr(k_out), _out_dt(fp8, dt), _ptr(q), _ptr(k), _ptr(wq), _ptr(wk), dt,
+            T, Hq, Hk, D, rotary_dim, layout, _ptr(positions), _ptr(cos), _ptr(sin), cache_len,
+            eps, weight_offset, inv_scale)
+    if unrounded:
+        _check(lib().edge_qk_norm_rope_ex(*args, QK_ROTATE_UNROUNDED, _stream(stream)),
+               "edge_qk_norm_rope_ex")
+    else:
+        _check(lib().edge_qk_norm_rope(*args, _stream(stream)), "edge_qk_norm_rope")
+    return q_out, k_out
+
+
+def rope(q, k, positions, cos, sin, *, rotary_dim=None, layout=ROTATE_HALF, q_out=None,
+         k_out=None, fp8=False, inv_scale=1.0, cache_len=None, stream=None):
+    """Standalone rotary embedding of q: [T, Hq, D] and k: [T, Hk, D] (k may
+    be None).  Pass q_out=q (k_out=k) for the in-place form.  Returns (q_out, k_out)."""
+    _need_contig(q, k, positions, cos, sin, q_out, k_out)
+    T, Hq, Hk, D, rotary_dim, cache_len, layout, q_out, k_out = _qk_shapes(
+        q, k, cos, rotary_dim, cache_len, layout, fp8, q_out, k_out)
+    dt = _dt(q)
+    _check(lib().edge_rope(_ptr(q_out), _ptr(k_out), _out_dt(fp8, dt), _ptr(q), _ptr(k), dt, T, Hq,
+                           Hk, D, rotary_dim, layout, _ptr(positions), _ptr(cos), _ptr(sin),
+                           cache_len, inv_scale, _stream(stream)), "edge_rope")
     return q_out, k_out

@@ -65,9 +65,9 @@ def _lib():
         L.oracle_rmsnorm.argtypes = [P, I, P, P, P, I, I64, I64, F, I, F]
         L.oracle_add_rmsnorm.argtypes = [P, I, P, P, P, P, P, I, I64, I64, F, I, F]
         L.oracle_glu_act.argtypes = [P, I, P, P, I, I64, I64, I, F]
-        L.oracle_rope.argtypes = [P, I, P, I, I64, I, I, I, I, P, P, P, I64]
+        L.oracle_rope.argtypes = [P, I, P, P, P, I, I64, I, I, I, I, P, P, P, I64, F]
         L.oracle_qk_norm_rope.argtypes = [P, P, I, P, P, P, P, P, P, P, P, P, P, P, P, I, I64, I,
-                                          I, I, I, I, P, P, P, I64, F, I, F, D]
+                                          I, I, I, I, P, P, P, I64, F, I, F, D, I]
         L.oracle_set_rotation_scale.argtypes = [D]
         for name in ("oracle_rmsnorm", "oracle_add_rmsnorm", "oracle_glu_act", "oracle_rope",
                      "oracle_qk_norm_rope", "oracle_version"):
@@ -180,20 +180,27 @@ def glu_act(gate_up, fmt, act, out_fmt=None, inv_scale=1.0):
     return out, pre
 
 
-def rope(x, fmt, rotary_dim, layout, positions, cos, sin, out_fmt=None):
-    """Standalone rotary embedding of x: [tokens, heads, head_dim] storage."""
+def rope(x, fmt, rotary_dim, layout, positions, cos, sin, out_fmt=None, inv_scale=1.0,
+         cache_len=None, diagnostics=False):
+    """Standalone rotary embedding of x: [tokens, heads, head_dim] storage.
+    With diagnostics=True returns (out, pre, mag): the exact values before the
+    output rounding and their error scale (the pair norm of rotated channels)."""
     out_fmt = fmt if out_fmt is None else out_fmt
     x = _c(x, STORAGE[fmt])
     tokens, heads, head_dim = x.shape
     positions = _c(np.asarray(positions, np.int64))
     cos = _c(cos, np.float32)
     sin = _c(sin, np.float32)
-    cache_len = 0 if cos is None else cos.shape[0]
+    if cache_len is None:
+        cache_len = 0 if cos is None else cos.shape[0]
     out = np.empty(x.shape, STORAGE[out_fmt])
-    rc = _lib().oracle_rope(_ptr(out), out_fmt, _ptr(x), fmt, tokens, heads, head_dim, rotary_dim,
-                            layout, _ptr(positions), _ptr(cos), _ptr(sin), cache_len)
+    pre = np.empty(x.shape) if diagnostics else None
+    mag = np.empty(x.shape) if diagnostics else None
+    rc = _lib().oracle_rope(_ptr(out), out_fmt, _ptr(pre), _ptr(mag), _ptr(x), fmt, tokens, heads,
+                            head_dim, rotary_dim, layout, _ptr(positions), _ptr(cos), _ptr(sin),
+                            cache_len, ctypes.c_float(inv_scale))
     _check(rc, "rope")
-    return out
+    return (out, pre, mag) if diagnostics else out
 
 
 class QKResult:
@@ -204,7 +211,8 @@ class QKResult:
 
 
 def qk_norm_rope(q, k, wq, wk, fmt, rotary_dim, layout, positions, cos, sin, eps,
-                 weight_offset=0, out_fmt=None, inv_scale=1.0, eta=2.0 ** -20, cache_len=None):
+                 weight_offset=0, out_fmt=None, inv_scale=1.0, eta=2.0 ** -20, cache_len=None,
+                 unrounded=False):
     """q: [T, Hq, D], k: [T, Hk, D] storage; cos/sin: [P, rotary_dim/2] fp32.
 
     Besides the outputs, returns per element the exact pre-rounding value
@@ -234,7 +242,7 @@ def qk_norm_rope(q, k, wq, wk, fmt, rotary_dim, layout, positions, cos, sin, eps
         _ptr(res.q_lo), _ptr(res.k_lo), _ptr(res.q_hi), _ptr(res.k_hi), _ptr(res.q_mag),
         _ptr(res.k_mag), _ptr(q), _ptr(k),
         _ptr(wq), _ptr(wk), fmt, T, Hq, Hk, D, rotary_dim, layout, _ptr(positions), _ptr(cos),
-        _ptr(sin), cache_len, eps, weight_offset, inv_scale, eta)
+        _ptr(sin), cache_len, eps, weight_offset, inv_scale, eta, 1 if unrounded else 0)
     _check(rc, "qk_norm_rope")
     return res
 

@@ -374,12 +374,15 @@ static void rotate(double a, double b, double c, double s, double* ra, double* r
     *rb = b * c + a * s;
 }
 
-/* Standalone rotary embedding of already-normalized heads x[tokens, heads, D]
- * (values in format f): rotate the first rho channels of every head of token
- * t by cos/sin row positions[t], round once to out_fmt. */
-int oracle_rope(void* out, int out_fmt, const void* x, int f, int64_t tokens, int heads,
-                int head_dim, int rotary_dim, int layout, const int64_t* positions,
-                const float* cos_cache, const float* sin_cache, int64_t cache_len)
+/* Standalone rotary embedding ([TEO] section 5.1, the rotary operator) of
+ * heads x[tokens, heads, D] (values in format f): rotate the first rho
+ * channels of every head of token t by cos/sin row positions[t] and round
+ * once to out_fmt (or take the FP8 epilogue).  A token whose position is
+ * outside the cache is copied unchanged. */
+int oracle_rope(void* out, int out_fmt, double* pre, double* mag, const void* x, int f,
+                int64_t tokens, int heads, int head_dim, int rotary_dim, int layout,
+                const int64_t* positions, const float* cos_cache, const float* sin_cache,
+                int64_t cache_len, float inv_scale)
 {
     if (!common_ok(out_fmt, f, tokens, head_dim, 0)) return 1;
     if (rotary_dim < 0 || rotary_dim > head_dim || (rotary_dim & 1)) return 1;
@@ -403,8 +406,19 @@ int oracle_rope(void* out, int out_fmt, const void* x, int f, int64_t tokens, in
                     y[ib] = rb;
                 }
             }
-            for (int i = 0; i < head_dim; ++i)
-                store(out, out_fmt, base + i, oracle_bits(oracle_round(y[i], out_fmt), out_fmt));
+            for (int i = 0; i < head_dim; ++i) {
+                store(out, out_fmt, base + i, emit(y[i], out_fmt, inv_scale));
+                if (pre) pre[base + i] = y[i];
+                if (mag) {
+                    double m2 = fabs(y[i]);
+                    if (rot && i < rotary_dim) {
+                        int partner = layout == OR_INTERLEAVED ? (i ^ 1)
+                                                               : (i < half ? i + half : i - half);
+                        m2 = sqrt(y[i] * y[i] + y[partner] * y[partner]);
+                    }
+                    mag[base + i] = m2;
+                }
+            }
         }
     }
     free(y);
@@ -442,8 +456,8 @@ static int near_tie(double v, int f, double eta, double* other)
 static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, const double* w, int f,
                      int64_t t, int heads, int D, int rho, int layout, int rot, int64_t p,
                      const float* cs, const float* sn, float eps, int delta, float inv_scale,
-                     double eta, double* xr, double* n, double* m, double* malt, int* tie,
-                     double* y, double* ylo, double* yhi)
+                     double eta, int unrounded, double* xr, double* n, double* m,
+                     double* malt, int* tie, double* y, double* ylo, double* yhi)
 {
     int half = rho / 2;
     for (int h = 0; h < heads; ++h) {
@@ -461,7 +475,18 @@ static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, const do
             ylo[i] = fmin(m[i], malt[i]);
             yhi[i] = fmax(m[i], malt[i]);
         }
-        if (rot) {
+        if (rot && unrounded) {
+            /* variant of the [NIN] review, item 1: the rotation consumes the
+             * normalized value itself, and the output is rounded once */
+            for (int j = 0; j < half; ++j) {
+                int ia, ib;
+                pair_index(layout, rho, j, &ia, &ib);
+                double c = (double)cs[p * half + j], s = (double)sn[p * half + j];
+                rotate(n[ia], n[ib], c, s, &y[ia], &y[ib]);
+                ylo[ia] = yhi[ia] = y[ia];
+                ylo[ib] = yhi[ib] = y[ib];
+            }
+        } else if (rot) {
             for (int j = 0; j < half; ++j) {
                 int ia, ib;
                 pair_index(layout, rho, j, &ia, &ib);
@@ -535,7 +560,7 @@ int oracle_qk_norm_rope(void* q_out, void* k_out, int out_fmt, double* q_pre, do
                         int64_t tokens, int q_heads, int k_heads, int head_dim, int rotary_dim,
                         int layout, const int64_t* positions, const float* cos_cache,
                         const float* sin_cache, int64_t cache_len, float eps, int weight_offset,
-                        float inv_scale, double eta)
+                        float inv_scale, double eta, int unrounded)
 {
     if (!common_ok(out_fmt, f, tokens, head_dim, weight_offset)) return 1;
     if (q_heads < 0 || k_heads < 0 || head_dim <= 0) return 1;
@@ -557,12 +582,12 @@ int oracle_qk_norm_rope(void* q_out, void* k_out, int out_fmt, double* q_pre, do
         int rot = rotary_dim > 0 && in_cache(p, cache_len);
         qk_heads(q_out, out_fmt, dq, q, wq ? wqr : NULL, f, t, q_heads, head_dim, rotary_dim,
                  layout, rot, p, cos_cache, sin_cache, eps, weight_offset, inv_scale, eta,
-                 buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd,
-                 buf + 6 * nd);
+                 unrounded, buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd,
+                 buf + 5 * nd, buf + 6 * nd);
         qk_heads(k_out, out_fmt, dk, k, wk ? wkr : NULL, f, t, k_heads, head_dim, rotary_dim,
                  layout, rot, p, cos_cache, sin_cache, eps, weight_offset, inv_scale, eta,
-                 buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd,
-                 buf + 6 * nd);
+                 unrounded, buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd,
+                 buf + 5 * nd, buf + 6 * nd);
     }
     free(wqr); free(wkr); free(buf); free(tie);
     return 0;

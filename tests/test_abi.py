@@ -87,6 +87,8 @@ def qk(L, qo=QO, ko=KO, out_dt=BF16, q=Q, k=K, wq=WQ, wk=WK, dt=BF16, T=4, Hq=8,
 
 
 def test_zero_rows_is_ok_and_launches_nothing(L):
+    assert L.edge_rope(QO, KO, BF16, Q, K, BF16, 0, 8, 2, 128, 64, 0, POS, COS, SIN, 4096, 1.0,
+                       None) == OK
     assert rms(L, rows=0) == OK
     assert add(L, rows=0) == OK
     assert glu(L, rows=0) == OK
@@ -129,6 +131,14 @@ def test_zero_rows_is_ok_and_launches_nothing(L):
     (lambda L: qk(L, pos=POS + 4), ALIGN),
     (lambda L: qk(L, cos=COS + 2), ALIGN),
     (lambda L: qk(L, D=4096, rot=64), UNSUP),
+    (lambda L: L.edge_qk_norm_rope_ex(QO, KO, BF16, Q, K, WQ, WK, BF16, 4, 8, 2, 128, 64, 0, POS,
+                                      COS, SIN, 4096, 1e-6, 1, 1.0, 2, None), VALUE),
+    (lambda L: L.edge_rope(QO, KO, BF16, None, K, BF16, 4, 8, 2, 128, 64, 0, POS, COS, SIN,
+                           4096, 1.0, None), NULL),
+    (lambda L: L.edge_rope(QO, KO, BF16, Q, K, BF16, 4, 8, 2, 128, 63, 0, POS, COS, SIN,
+                           4096, 1.0, None), SHAPE),
+    (lambda L: L.edge_rope(Q + 2, KO, BF16, Q, K, BF16, 4, 8, 2, 128, 64, 0, POS, COS, SIN,
+                           4096, 1.0, None), ALIAS),
     (lambda L: rms(L, hidden=2 ** 25, rows=1), UNSUP),
 ])
 def test_invalid_calls_are_rejected(L, call, status):

@@ -496,3 +496,89 @@ def test_runs_on_a_side_stream_and_in_a_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(qo, ref_q) and torch.equal(ko, ref_k)
     assert c["T"] == 8
+
+
+# ---------------------------------------------------------------- standalone rotary
+
+ROPE_CASES = {
+    "bf16_partial_rotate_half": dict(dtype=torch.bfloat16, T=37, Hq=16, Hk=2, D=256, rot=64,
+                                     layout=0, P=64, positions=np.r_[np.arange(34), [64, -1, 63]]),
+    "f16_full_interleaved_in_place": dict(dtype=torch.float16, T=19, Hq=16, Hk=8, D=256, rot=256,
+                                          layout=1, P=4096, positions="arange", inplace=True),
+    "f32_full_rotate_half": dict(dtype=torch.float32, T=5, Hq=8, Hk=2, D=128, rot=128, layout=0,
+                                 P=4096, positions="cfg_out_of_cache"),
+    "many_heads_bf16": dict(dtype=torch.bfloat16, T=900, Hq=24, Hk=4, D=256, rot=64, layout=0,
+                            P=32768, positions="offset"),
+    "many_heads_interleaved": dict(dtype=torch.bfloat16, T=1000, Hq=16, Hk=8, D=256, rot=256,
+                                   layout=1, P=4096, positions="arange"),
+    "generic_d96": dict(dtype=torch.bfloat16, T=9, Hq=3, Hk=1, D=96, rot=40, layout=0, P=16,
+                        positions="arange"),
+    "no_k": dict(dtype=torch.bfloat16, T=7, Hq=4, Hk=0, D=128, rot=64, layout=0, P=16,
+                 positions="arange"),
+}
+
+
+def run_rope(c, fp8=False):
+    dtype, fmt = c["dtype"], TORCH_FMT[c["dtype"]]
+    inp = synth.qk_inputs(0, dtype, c["T"], c["Hq"], c["Hk"], c["D"], c["rot"], theta=1e6,
+                          cache_len=c["P"], positions=c["positions"])
+    out_fmt = oracle.E4M3 if fp8 else fmt
+    inv = 448.0 / 6.0
+    pos, cs, sn = inp["positions"].numpy(), storage(inp["cos"]), storage(inp["sin"])
+    refs = [oracle.rope(storage(inp[n]), fmt, c["rot"], c["layout"], pos, cs, sn,
+                        out_fmt=out_fmt, inv_scale=inv, diagnostics=True) for n in ("q", "k")]
+    q, k = dev(inp["q"]), dev(inp["k"])
+    odt = torch.uint8 if fp8 else dtype
+    if c.get("inplace") and not fp8:
+        gq, gk = Guarded(q.shape, dtype), Guarded(k.shape, dtype)
+        gq.t.copy_(q)
+        gk.t.copy_(k)
+        q, k = gq.t, gk.t
+    else:
+        gq, gk = Guarded(q.shape, odt), Guarded(k.shape, odt)
+    edge_ops.rope(q, k, dev(inp["positions"]), dev(inp["cos"]), dev(inp["sin"]),
+                  rotary_dim=c["rot"], layout=c["layout"], q_out=gq.t, k_out=gk.t, fp8=fp8,
+                  inv_scale=inv, cache_len=c["P"])
+    torch.cuda.synchronize()
+    gq.check()
+    gk.check()
+    for name, g, (ref, pre, mag) in (("q", gq, refs[0]), ("k", gk, refs[1])):
+        if ref.size:
+            check_out(name, storage(g.t.cpu()), ref, pre, mag, fmt, out_fmt, ETA_NORM, inv)
+
+
+@pytest.mark.parametrize("name", list(ROPE_CASES))
+def test_rope(name):
+    run_rope(ROPE_CASES[name])
+
+
+@pytest.mark.parametrize("name", ["bf16_partial_rotate_half", "many_heads_interleaved",
+                                  "f32_full_rotate_half"])
+def test_rope_fp8(name):
+    run_rope(ROPE_CASES[name], fp8=True)
+
+
+# ---------------------------------------------------------------- review variant
+
+@pytest.mark.parametrize("name", ["cfg3_16_2_T333", "cfg4_bf16", "cfg1_f32", "generic_rot24",
+                                  "quad_cfg4_interleaved", "d128_bf16", "generic_odd_d37"])
+def test_qk_norm_rope_unrounded(name):
+    # rotation of the fp32 normalized value, one rounding (ninfer review, item 1)
+    c = QK_CASES[name]
+    dtype, fmt = c["dtype"], TORCH_FMT[c["dtype"]]
+    inp = synth.qk_inputs(0, dtype, c["T"], c["Hq"], c["Hk"], c["D"], c["rot"],
+                          theta=c["theta"], cache_len=c["P"], positions=c["positions"],
+                          w_mean=c["w_mean"] or 0.0, w_std=c["w_std"])
+    ref = oracle.qk_norm_rope(storage(inp["q"]), storage(inp["k"]), storage(inp["wq"]),
+                              storage(inp["wk"]), fmt, c["rot"], c["layout"],
+                              inp["positions"].numpy(), storage(inp["cos"]), storage(inp["sin"]),
+                              1e-6, c["offset"], eta=ETA_NORM, unrounded=True)
+    d = {n: dev(inp[n]) for n in ("q", "k", "wq", "wk", "positions", "cos", "sin")}
+    qo, ko = edge_ops.qk_norm_rope(d["q"], d["k"], d["wq"], d["wk"], d["positions"], d["cos"],
+                                   d["sin"], rotary_dim=c["rot"], layout=c["layout"], eps=1e-6,
+                                   weight_offset=c["offset"], cache_len=c["P"], unrounded=True)
+    torch.cuda.synchronize()
+    check_out(name + " q", storage(qo.cpu()), ref.q_out, ref.q_pre, ref.q_mag, fmt, fmt,
+              ETA_NORM, lo=ref.q_lo, hi=ref.q_hi)
+    check_out(name + " k", storage(ko.cpu()), ref.k_out, ref.k_pre, ref.k_mag, fmt, fmt,
+              ETA_NORM, lo=ref.k_lo, hi=ref.k_hi)

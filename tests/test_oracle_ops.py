@@ -414,3 +414,63 @@ def test_tie_bounds_bracket_the_exact_value():
     assert 0 < wide < 0.2 * (r.q_lo.size + r.k_lo.size)
     # pass-through channels of a bf16/fp16 output round n itself: no interval
     assert np.array_equal(r.q_lo[..., 32:], r.q_hi[..., 32:])
+
+
+# ----------------------------------------------------------------- review variant and standalone rope
+
+@pytest.mark.parametrize("layout", [oracle.ROTATE_HALF, oracle.INTERLEAVED])
+def test_unrounded_variant_rotates_the_exact_normalized_value(layout):
+    # the ninfer review (item 1): rotate the fp32 RMSNorm result and round once.
+    # Pin: torch fp64 rms_norm, then complex multiplication, then one rounding.
+    T, H, D, rho = 6, 3, 64, 32
+    inp = synth.qk_inputs(4, torch.bfloat16, T, H, 1, D, rho, theta=1e4, cache_len=64,
+                          positions=np.array([0, 3, 9, 63, 64, -1]), w_std=0.1)
+    r = oracle.qk_norm_rope(storage(inp["q"]), storage(inp["k"]), storage(inp["wq"]),
+                            storage(inp["wk"]), oracle.BF16, rho, layout, inp["positions"].numpy(),
+                            storage(inp["cos"]), storage(inp["sin"]), 1e-6, 1, unrounded=True)
+    x64 = torch.from_numpy(dec(inp["q"]))
+    w64 = torch.from_numpy(dec(inp["wq"])) + 1.0
+    n = F.rms_norm(x64, (D,), weight=w64, eps=E32(1e-6)).numpy()
+    half = rho // 2
+    ia, ib = (np.arange(half), np.arange(half) + half) if layout == oracle.ROTATE_HALF else \
+        (2 * np.arange(half), 2 * np.arange(half) + 1)
+    ref = n.copy()
+    pos = inp["positions"].numpy()
+    for t in range(T):
+        if 0 <= pos[t] < 64:
+            e = (inp["cos"].double().numpy()[pos[t]] + 1j * inp["sin"].double().numpy()[pos[t]])
+            z = (n[t][:, ia] + 1j * n[t][:, ib]) * e
+            ref[t][:, ia], ref[t][:, ib] = z.real, z.imag
+    np.testing.assert_allclose(r.q_pre, ref, rtol=1e-12, atol=1e-15)
+    assert np.array_equal(r.q_out, oracle.encode(ref, oracle.BF16))
+    # the rounded (default) form differs somewhere in the rotated channels only
+    r0 = oracle.qk_norm_rope(storage(inp["q"]), storage(inp["k"]), storage(inp["wq"]),
+                             storage(inp["wk"]), oracle.BF16, rho, layout, pos,
+                             storage(inp["cos"]), storage(inp["sin"]), 1e-6, 1)
+    assert np.array_equal(r0.q_out[..., rho:], r.q_out[..., rho:])
+
+
+def test_unrounded_and_rounded_differ_somewhere():
+    inp, r0 = _qk(torch.bfloat16, T=32, Hq=8, Hk=2, D=128, rho=128, positions="arange",
+                  cache_len=64)
+    a = [storage(inp[n]) for n in ("q", "k", "wq", "wk")]
+    r1 = oracle.qk_norm_rope(*a, oracle.BF16, 128, oracle.ROTATE_HALF, inp["positions"].numpy(),
+                             storage(inp["cos"]), storage(inp["sin"]), 1e-6, 1, unrounded=True)
+    assert np.count_nonzero(r0.q_out != r1.q_out) > 0
+
+
+def test_rope_diagnostics_and_fp8():
+    T, H, D, rho = 4, 2, 32, 16
+    rng = np.random.default_rng(9)
+    x = torch.from_numpy(rng.standard_normal((T, H, D)).astype(np.float32)).to(torch.bfloat16)
+    cos, sin = synth.rope_cache(1e4, rho, 8)
+    pos = np.array([0, 5, 7, 8])
+    out, pre, mag = oracle.rope(storage(x), oracle.BF16, rho, oracle.ROTATE_HALF, pos,
+                                storage(cos), storage(sin), diagnostics=True)
+    assert np.array_equal(out, oracle.encode(pre, oracle.BF16))
+    assert np.all(mag >= np.abs(pre))
+    # out-of-cache token (position 8 with 8 rows) is copied unchanged
+    assert np.array_equal(out[3], storage(x)[3])
+    q8 = oracle.rope(storage(x), oracle.BF16, rho, oracle.ROTATE_HALF, pos, storage(cos),
+                     storage(sin), out_fmt=oracle.E4M3, inv_scale=16.0)
+    assert np.array_equal(q8, oracle.quantize(pre, 16.0))

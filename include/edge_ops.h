@@ -177,6 +177,30 @@ edge_status edge_qk_norm_rope(void* q_out, void* k_out, edge_dtype out_dt, const
                               int64_t cache_len, float eps, int weight_offset, float inv_scale,
                               void* stream);
 
+/*
+ * One-read LayerNorm (FlashRT "optimization-details": siglip_layernorm_1read,
+ * a single pass over a register-cached row instead of three).
+ *
+ *   out[t, i] = (x[t, i] - mu_t) / sqrt(var_t + eps) * gamma[i] + beta[i]
+ *   mu_t = mean_i x[t, i],  var_t = mean_i (x[t, i] - mu_t)^2  (biased)
+ *
+ * x: [rows, hidden] of dt.  gamma, beta: [hidden] of dt, each nullable (1, 0).
+ * out: [rows, hidden] of out_dt; out == x is allowed when out_dt == dt.
+ * fp32 arithmetic, one rounding (or the FP8 epilogue).
+ */
+edge_status edge_layernorm(void* out, edge_dtype out_dt, const void* x, const void* gamma,
+                           const void* beta, edge_dtype dt, int64_t rows, int64_t hidden,
+                           float eps, float inv_scale, void* stream);
+
+/*
+ * Standalone static-scale FP8 quantization (FlashRT "optimization-details":
+ * quantize_fp8_static).  out[i] = E4M3(fl32(x[i]) * inv_scale), to nearest
+ * even with saturation to +-448.  x: n elements of dt.  out: n bytes, which
+ * must not overlap x.  inv_scale must be finite and > 0.
+ */
+edge_status edge_quantize_fp8(void* out, const void* x, edge_dtype dt, int64_t n, float inv_scale,
+                              void* stream);
+
 /* Flags of edge_qk_norm_rope_ex. */
 enum {
     /* Rotate the fp32 normalized value and round once after the rotation,

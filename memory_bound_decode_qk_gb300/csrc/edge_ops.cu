@@ -163,6 +163,8 @@ edge_status rows_entry(void* out, edge_dtype out_dt, const void* x, void* residu
     a.x = x;
     a.residual = fused ? residual : nullptr;
     a.w = w;
+    a.beta = nullptr;
+    a.layernorm = 0;
     a.out = out;
     a.rows = rows;
     a.hidden = hidden;
@@ -272,6 +274,70 @@ edge_status edge_add_rmsnorm(void* out, edge_dtype out_dt, const void* x, void* 
                              int weight_offset, float inv_scale, void* stream) {
     return rows_entry(out, out_dt, x, residual, true, w, dt, rows, hidden, eps, weight_offset,
                       inv_scale, stream);
+}
+
+edge_status edge_layernorm(void* out, edge_dtype out_dt, const void* x, const void* gamma,
+                           const void* beta, edge_dtype dt, int64_t rows, int64_t hidden,
+                           float eps, float inv_scale, void* stream) {
+    edge_status st = check_out_dt(out_dt, dt);
+    if (st != EDGE_OK) return st;
+    if (x == nullptr || out == nullptr) return EDGE_ERR_NULL;
+    if (rows < 0 || hidden <= 0) return EDGE_ERR_SHAPE;
+    if (!finite_nonneg(eps)) return EDGE_ERR_VALUE;
+    if ((st = check_scale(out_dt, inv_scale)) != EDGE_OK) return st;
+    int64_t in_bytes = 0, out_bytes = 0;
+    if (!checked_bytes(rows, hidden, esize(dt), &in_bytes) ||
+        !checked_bytes(rows, hidden, esize(out_dt), &out_bytes)) {
+        return EDGE_ERR_SHAPE;
+    }
+    if (hidden > edge::kMaxHidden) return EDGE_ERR_UNSUPPORTED;
+    const int64_t es = esize(dt);
+    if (!aligned(x, es) || !aligned(gamma, es) || !aligned(beta, es) ||
+        !aligned(out, esize(out_dt))) {
+        return EDGE_ERR_ALIGN;
+    }
+    const Span so = span(out, out_bytes);
+    if (bad_alias(so, span(x, in_bytes), out_dt == dt) || overlap(so, span(gamma, hidden * es)) ||
+        overlap(so, span(beta, hidden * es))) {
+        return EDGE_ERR_ALIAS;
+    }
+    if (rows == 0) return EDGE_OK;
+    edge::RowsArgs a;
+    a.x = x;
+    a.residual = nullptr;
+    a.w = gamma;
+    a.beta = beta;
+    a.layernorm = 1;
+    a.out = out;
+    a.rows = rows;
+    a.hidden = hidden;
+    a.dt = (int)dt;
+    a.out_dt = (int)out_dt;
+    a.eps = eps;
+    a.inv_scale = inv_scale;
+    a.weight_offset = 0;
+    return finish(edge::launch_rows(a, static_cast<cudaStream_t>(stream)));
+}
+
+edge_status edge_quantize_fp8(void* out, const void* x, edge_dtype dt, int64_t n, float inv_scale,
+                              void* stream) {
+    if (!act_dtype(dt)) return EDGE_ERR_DTYPE;
+    if (out == nullptr || x == nullptr) return EDGE_ERR_NULL;
+    if (n < 0) return EDGE_ERR_SHAPE;
+    if (!(std::isfinite(inv_scale) && inv_scale > 0.0f)) return EDGE_ERR_VALUE;
+    int64_t in_bytes = 0;
+    if (!checked_bytes(n, 1, esize(dt), &in_bytes)) return EDGE_ERR_SHAPE;
+    if (n > edge::kMaxUnits * 8) return EDGE_ERR_UNSUPPORTED;
+    if (!aligned(x, esize(dt))) return EDGE_ERR_ALIGN;
+    if (overlap(span(out, n), span(x, in_bytes))) return EDGE_ERR_ALIAS;
+    if (n == 0) return EDGE_OK;
+    edge::QuantArgs a;
+    a.x = x;
+    a.out = out;
+    a.n = n;
+    a.dt = (int)dt;
+    a.inv_scale = inv_scale;
+    return finish(edge::launch_quant(a, static_cast<cudaStream_t>(stream)));
 }
 
 edge_status edge_glu_act(void* out, edge_dtype out_dt, const void* gate_up, edge_dtype dt,

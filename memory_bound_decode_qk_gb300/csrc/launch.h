@@ -32,7 +32,9 @@ struct QKArgs {
 struct RowsArgs {
     const void* x;
     void* residual;          // nullptr: plain RMSNorm
-    const void* w;           // nullable
+    const void* w;           // nullable (LayerNorm: gamma)
+    const void* beta;        // LayerNorm only, nullable
+    int layernorm;           // 1: LayerNorm (no residual)
     void* out;
     int64_t rows;
     int64_t hidden;
@@ -58,6 +60,15 @@ constexpr int64_t kMaxUnits = (int64_t(1) << 31) - 1;
 cudaError_t launch_qk(const QKArgs& a, cudaStream_t s);
 cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s);
 cudaError_t launch_glu(const GluArgs& a, cudaStream_t s);
+
+struct QuantArgs {
+    const void* x;
+    void* out;
+    int64_t n;
+    int dt;
+    float inv_scale;
+};
+cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();

@@ -1,0 +1,73 @@
+// quant.cu -- standalone static-scale FP8 E4M3 quantization (sm_103a).
+//
+// What it computes (FlashRT "optimization-details", quantize_fp8_static: the
+// input of the O projection): out[i] = E4M3(fl32(x[i]) * inv_scale), rounded
+// to nearest even with saturation to +-448.  The same fp32 decision as the
+// fused epilogue of the other ops.
+//
+// GB300 design: a pure stream of 2 (bf16/fp16) or 4 (fp32) bytes in and 1
+// byte out per element.  Each thread turns one 16-byte input vector into 8
+// (or 4) codes and writes them in one 8- (or 4-) byte store, in a one-shot
+// grid.  Elements past the last whole vector, or a misaligned tensor, go
+// through a scalar loop.
+#include "edge_common.cuh"
+#include "launch.h"
+
+namespace edge {
+namespace {
+
+template <typename T>
+__global__ void __launch_bounds__(256) quant_kernel(const char* x, uint8_t* out, int64_t n,
+                                                    int64_t nvec, float inv) {
+    constexpr int N = vec_elems<T>();
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t i = tid; i < nvec; i += stride) {
+        float y[N];
+        unpack_vec<T, N>(__ldcs(reinterpret_cast<const uint4*>(x) + i), y);
+        auto q8 = quantize_vec<N>(y, inv);
+        reinterpret_cast<decltype(q8)*>(out)[i] = q8;
+    }
+    for (int64_t i = nvec * N + tid; i < n; i += stride) {
+        out[i] = quantize1(to_f(reinterpret_cast<const T*>(x)[i]), inv);
+    }
+}
+
+template <typename T>
+cudaError_t launch_typed(const QuantArgs& a, cudaStream_t s) {
+    constexpr int N = vec_elems<T>();
+    const bool vec = (reinterpret_cast<uintptr_t>(a.x) % 16) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.out) % N) == 0;
+    const int64_t nvec = vec ? a.n / N : 0;
+    const int64_t work = nvec > 0 ? nvec : a.n;
+    const int threads = 256;
+    int64_t blocks = (work + threads - 1) / threads;
+    const int64_t cap = (int64_t)sm_count() * 64;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    return cudaLaunchKernelEx(&cfg, quant_kernel<T>, static_cast<const char*>(a.x),
+                              static_cast<uint8_t*>(a.out), a.n, nvec, a.inv_scale);
+}
+
+}  // namespace
+
+cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
+    switch (a.dt) {
+        case kF32: return launch_typed<float>(a, s);
+        case kF16: return launch_typed<__half>(a, s);
+        default: return launch_typed<__nv_bfloat16>(a, s);
+    }
+}
+
+}  // namespace edge

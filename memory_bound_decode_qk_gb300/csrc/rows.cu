@@ -28,7 +28,8 @@ namespace {
 struct RowsP {
     const char* x;
     char* res;
-    const char* w;
+    const char* w;          // RMSNorm weight, or LayerNorm gamma
+    const char* beta;       // LayerNorm beta (nullable)
     char* out;
     int64_t rows;
     int hidden;
@@ -170,12 +171,181 @@ __global__ void __launch_bounds__(256) rows_generic_kernel(RowsP p) {
     }
 }
 
-template <typename T, bool FP8, bool ADD>
-cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
+// Sum of v over the W warps that own a row (one shuffle tree per warp, then
+// shared memory).  Every thread of the CTA calls it the same number of times.
+__device__ __forceinline__ float row_sum(float v, const RowsP& p, int g, int lane, int wib,
+                                         float* red) {
+    v = group_sum<32>(v);
+    if (p.W > 1) {
+        if (lane == 0) red[wib] = v;
+        __syncthreads();
+        v = 0.0f;
+        for (int k = 0; k < p.W; ++k) v = __fadd_rn(v, red[g * p.W + k]);
+        __syncthreads();
+    }
+    return v;
+}
+
+// One-read LayerNorm (FlashRT siglip_layernorm_1read): the row stays in
+// registers for the mean, the variance of the centred values and the
+// output, so x is read from HBM once.  y = (x - mu) r gamma + beta.
+template <typename T, bool FP8, int V>
+__global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
+    constexpr int N = vec_elems<T>();
+    __shared__ float red[16];
+    const int tpr = 32 * p.W;
+    const int g = threadIdx.x / tpr;
+    const int tid = threadIdx.x - g * tpr;
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int64_t in_row = (int64_t)p.hidden * (int64_t)sizeof(T);
+    const int64_t out_row = FP8 ? (int64_t)p.hidden : in_row;
+    const uint4* gv = reinterpret_cast<const uint4*>(p.w);
+    const uint4* bv = reinterpret_cast<const uint4*>(p.beta);
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (int64_t r0 = (int64_t)blockIdx.x * p.RPB; r0 < p.rows; r0 += (int64_t)gridDim.x * p.RPB) {
+        const int64_t row = r0 + g;
+        const bool active = row < p.rows;
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + (active ? row : r0) * in_row);
+        uint4 xv[V], gr[V], br[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int idx = tid + i * tpr;
+            const bool ok = active && idx < p.nvec;
+            xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+            gr[i] = (ok && gv != nullptr) ? __ldg(gv + idx) : make_uint4(0u, 0u, 0u, 0u);
+            br[i] = (ok && bv != nullptr) ? __ldg(bv + idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float a[N];
+            unpack_vec<T, N>(xv[i], a);
+#pragma unroll
+            for (int e = 0; e < N; ++e) sum = __fadd_rn(sum, a[e]);
+        }
+        const float mu = __fmul_rn(row_sum(sum, p, g, lane, wib, red), p.invH);
+        float sq = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int idx = tid + i * tpr;
+            if (!(active && idx < p.nvec)) continue;  // padding lanes add nothing
+            float a[N];
+            unpack_vec<T, N>(xv[i], a);
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                const float d = __fsub_rn(a[e], mu);
+                sq = __fmaf_rn(d, d, sq);
+            }
+        }
+        const float r = inv_rms(row_sum(sq, p, g, lane, wib, red), p.invH, p.eps);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int idx = tid + i * tpr;
+            if (!(active && idx < p.nvec)) continue;
+            float a[N], gg[N], bb[N], y[N];
+            unpack_vec<T, N>(xv[i], a);
+            if (gv != nullptr) unpack_vec<T, N>(gr[i], gg);
+            if (bv != nullptr) unpack_vec<T, N>(br[i], bb);
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                float v = __fmul_rn(__fsub_rn(a[e], mu), r);
+                if (gv != nullptr) v = __fmul_rn(v, gg[e]);
+                if (bv != nullptr) v = __fadd_rn(v, bb[e]);
+                y[e] = v;
+            }
+            char* orow = p.out + row * out_row;
+            if constexpr (FP8) {
+                auto q8 = quantize_vec<N>(y, p.inv);
+                reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
+            } else {
+                reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
+            }
+        }
+    }
+}
+
+// Any size or alignment: one CTA per row, three passes (the second and third
+// hit L1/L2).
+template <typename T, bool FP8>
+__global__ void __launch_bounds__(256) ln_generic_kernel(RowsP p) {
+    __shared__ float red[8];
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    auto block_sum = [&](float v) {
+        v = group_sum<32>(v);
+        if (lane == 0) red[wib] = v;
+        __syncthreads();
+        v = 0.0f;
+        for (int k = 0; k < nw; ++k) v = __fadd_rn(v, red[k]);
+        __syncthreads();
+        return v;
+    };
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const T* gm = reinterpret_cast<const T*>(p.w);
+    const T* bt = reinterpret_cast<const T*>(p.beta);
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const T* x = reinterpret_cast<const T*>(p.x) + row * p.hidden;
+        float sum = 0.0f;
+        for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) sum = __fadd_rn(sum, to_f(x[i]));
+        const float mu = __fmul_rn(block_sum(sum), p.invH);
+        float sq = 0.0f;
+        for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
+            const float d = __fsub_rn(to_f(x[i]), mu);
+            sq = __fmaf_rn(d, d, sq);
+        }
+        const float r = inv_rms(block_sum(sq), p.invH, p.eps);
+        for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
+            float v = __fmul_rn(__fsub_rn(to_f(x[i]), mu), r);
+            if (gm != nullptr) v = __fmul_rn(v, to_f(gm[i]));
+            if (bt != nullptr) v = __fadd_rn(v, to_f(bt[i]));
+            if constexpr (FP8) {
+                reinterpret_cast<uint8_t*>(p.out)[row * p.hidden + i] = quantize1(v, p.inv);
+            } else {
+                reinterpret_cast<T*>(p.out)[row * p.hidden + i] = from_f<T>(v);
+            }
+        }
+    }
+}
+
+// Launch shape of the vector kernels: W warps per row, V vectors per thread,
+// RPB rows per CTA.  false when the row needs the generic kernel.
+template <typename T, bool FP8>
+bool vec_shape(const RowsArgs& a, int sms, RowsP& p, int& V) {
     constexpr int N = vec_elems<T>();
     auto aligned = [](const void* ptr, uintptr_t n) {
         return ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) % n) == 0;
     };
+    const bool vec_ok = (a.hidden * (int64_t)sizeof(T)) % 16 == 0 && aligned(a.x, 16) &&
+                        aligned(a.residual, 16) && aligned(a.w, 16) && aligned(a.beta, 16) &&
+                        aligned(a.out, FP8 ? N : 16);
+    const int64_t nvec = a.hidden / N;
+    if (!vec_ok || nvec > 16 * 32 * 8) return false;
+    // target vectors per thread (measured on GB300: 1 for few rows, 2 for
+    // many; more per thread lowers occupancy and loses bandwidth)
+    int vt = a.rows >= 2 * sms ? 2 : 1;
+    if (rows_vt_override() > 0) vt = rows_vt_override();
+    int W = (int)((nvec + 32 * vt - 1) / (32 * vt));
+    if (W > 16) W = 16;
+    const int64_t per = (nvec + 32 * W - 1) / (32 * W);
+    V = per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
+    int RPB = 256 / (32 * W);
+    if (RPB < 1) RPB = 1;
+    p.nvec = (int)nvec;
+    p.W = W;
+    p.RPB = RPB;
+    return true;
+}
+
+template <typename T, bool FP8, bool ADD>
+cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
     const int sms = sm_count();
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -185,32 +355,22 @@ cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
 
-    const bool vec_ok = (a.hidden * (int64_t)sizeof(T)) % 16 == 0 && aligned(a.x, 16) &&
-                        aligned(a.residual, 16) && aligned(a.w, 16) &&
-                        aligned(a.out, FP8 ? N : 16);
-    const int64_t nvec = a.hidden / N;
-    if (vec_ok && nvec <= 16 * 32 * 8) {
-        // vectors per thread: many rows -> more bytes in flight per thread;
-        // few rows -> spread each row over more warps
-        // target vectors per thread (measured on GB300: 1 for few rows, 2 for
-        // many; more per thread lowers occupancy and loses bandwidth)
-        int vt = a.rows >= 2 * sms ? 2 : 1;
-        if (rows_vt_override() > 0) vt = rows_vt_override();
-        int W = (int)((nvec + 32 * vt - 1) / (32 * vt));
-        if (W > 16) W = 16;
-        const int64_t per = (nvec + 32 * W - 1) / (32 * W);
-        int V = per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
-        int RPB = 256 / (32 * W);
-        if (RPB < 1) RPB = 1;
-        p.nvec = (int)nvec;
-        p.W = W;
-        p.RPB = RPB;
-        const int threads = 32 * W * RPB;
-        int64_t blocks = (a.rows + RPB - 1) / RPB;
+    int V = 1;
+    if (vec_shape<T, FP8>(a, sms, p, V)) {
+        const int threads = 32 * p.W * p.RPB;
+        int64_t blocks = (a.rows + p.RPB - 1) / p.RPB;
         const int64_t cap = (int64_t)sms * (2048 / threads) * 8;
         if (blocks > cap) blocks = cap;
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(threads);
+        if (a.layernorm) {
+            switch (V) {
+                case 1: return cudaLaunchKernelEx(&cfg, ln_vec_kernel<T, FP8, 1>, p);
+                case 2: return cudaLaunchKernelEx(&cfg, ln_vec_kernel<T, FP8, 2>, p);
+                case 4: return cudaLaunchKernelEx(&cfg, ln_vec_kernel<T, FP8, 4>, p);
+                default: return cudaLaunchKernelEx(&cfg, ln_vec_kernel<T, FP8, 8>, p);
+            }
+        }
         switch (V) {
             case 1: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 1>, p);
             case 2: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 2>, p);
@@ -223,6 +383,7 @@ cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
     if (blocks > cap) blocks = cap;
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(256);
+    if (a.layernorm) return cudaLaunchKernelEx(&cfg, ln_generic_kernel<T, FP8>, p);
     return cudaLaunchKernelEx(&cfg, rows_generic_kernel<T, FP8, ADD>, p);
 }
 
@@ -232,6 +393,7 @@ cudaError_t launch_dt(const RowsArgs& a, RowsP& p, cudaStream_t s) {
     const bool add = a.residual != nullptr;
     if (fp8) return add ? launch_typed<T, true, true>(a, p, s) : launch_typed<T, true, false>(a, p, s);
     return add ? launch_typed<T, false, true>(a, p, s) : launch_typed<T, false, false>(a, p, s);
+    // (LayerNorm takes the ADD = false instantiation of launch_typed)
 }
 
 }  // namespace
@@ -241,6 +403,7 @@ cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s) {
     p.x = static_cast<const char*>(a.x);
     p.res = static_cast<char*>(a.residual);
     p.w = static_cast<const char*>(a.w);
+    p.beta = static_cast<const char*>(a.beta);
     p.out = static_cast<char*>(a.out);
     p.rows = a.rows;
     p.hidden = (int)a.hidden;

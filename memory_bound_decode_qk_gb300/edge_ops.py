@@ -25,8 +25,8 @@ STATUS = {
     8: "EDGE_ERR_VALUE",
 }
 EXPORTS = ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope",
-           "edge_qk_norm_rope_ex", "edge_rope", "edge_status_str", "edge_last_cuda_error",
-           "edge_version")
+           "edge_qk_norm_rope_ex", "edge_rope", "edge_layernorm", "edge_quantize_fp8",
+           "edge_status_str", "edge_last_cuda_error", "edge_version")
 QK_ROTATE_UNROUNDED = 1
 
 _DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
@@ -70,8 +70,10 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
     L.edge_qk_norm_rope_ex.argtypes = [P, P, I, P, P, P, P, I, I64, I32, I32, I32, I32, I, P, P,
                                        P, I64, F, I, F, ctypes.c_uint32, P]
     L.edge_rope.argtypes = [P, P, I, P, P, I, I64, I32, I32, I32, I32, I, P, P, P, I64, F, P]
+    L.edge_layernorm.argtypes = [P, I, P, P, P, I, I64, I64, F, F, P]
+    L.edge_quantize_fp8.argtypes = [P, P, I, I64, F, P]
     for name in ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope",
-                 "edge_qk_norm_rope_ex", "edge_rope"):
+                 "edge_qk_norm_rope_ex", "edge_rope", "edge_layernorm", "edge_quantize_fp8"):
         getattr(L, name).restype = I
     L.edge_status_str.argtypes = [I]
     L.edge_status_str.restype = ctypes.c_char_p
@@ -143,6 +145,30 @@ def add_rmsnorm(x, residual, w=None, *, eps=1e-6, weight_offset=0, out=None, fp8
     _check(lib().edge_add_rmsnorm(_ptr(out), _out_dt(fp8, dt), _ptr(x), _ptr(residual), _ptr(w),
                                   dt, rows, hidden, eps, weight_offset, inv_scale,
                                   _stream(stream)), "edge_add_rmsnorm")
+    return out
+
+
+def layernorm(x, gamma=None, beta=None, *, eps=1e-6, out=None, fp8=False, inv_scale=1.0,
+              stream=None):
+    """One-read LayerNorm over the last dim of x ([rows, hidden])."""
+    _need_contig(x, gamma, beta, out)
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    if out is None:
+        out = _alloc(x, x.shape, fp8)
+    dt = _dt(x)
+    _check(lib().edge_layernorm(_ptr(out), _out_dt(fp8, dt), _ptr(x), _ptr(gamma), _ptr(beta), dt,
+                                rows, hidden, eps, inv_scale, _stream(stream)), "edge_layernorm")
+    return out
+
+
+def quantize_fp8(x, inv_scale, *, out=None, stream=None):
+    """Static-scale E4M3 codes of x (any shape, contiguous); uint8 output."""
+    _need_contig(x, out)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib().edge_quantize_fp8(_ptr(out), _ptr(x), _dt(x), x.numel(), inv_scale,
+                                   _stream(stream)), "edge_quantize_fp8")
     return out
 
 

@@ -68,9 +68,12 @@ def _lib():
         L.oracle_rope.argtypes = [P, I, P, P, P, I, I64, I, I, I, I, P, P, P, I64, F]
         L.oracle_qk_norm_rope.argtypes = [P, P, I, P, P, P, P, P, P, P, P, P, P, P, P, I, I64, I,
                                           I, I, I, I, P, P, P, I64, F, I, F, D, I]
+        L.oracle_layernorm.argtypes = [P, I, P, P, P, P, P, I, I64, I64, F, F]
+        L.oracle_quantize_static.argtypes = [P, P, I, I64, F]
         L.oracle_set_rotation_scale.argtypes = [D]
         for name in ("oracle_rmsnorm", "oracle_add_rmsnorm", "oracle_glu_act", "oracle_rope",
-                     "oracle_qk_norm_rope", "oracle_version"):
+                     "oracle_qk_norm_rope", "oracle_layernorm", "oracle_quantize_static",
+                     "oracle_version"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -164,6 +167,31 @@ def add_rmsnorm(x, residual, w, fmt, eps, weight_offset=0, out_fmt=None, inv_sca
                                    inv_scale)
     _check(rc, "add_rmsnorm")
     return out, res, pre
+
+
+def layernorm(x, gamma, beta, fmt, eps, out_fmt=None, inv_scale=1.0):
+    """x: [rows, hidden] storage.  Returns (out storage, exact values, error scale)."""
+    out_fmt = fmt if out_fmt is None else out_fmt
+    x = _c(x, STORAGE[fmt])
+    gamma = _c(gamma, STORAGE[fmt])
+    beta = _c(beta, STORAGE[fmt])
+    rows, hidden = x.shape
+    out = np.empty(x.shape, STORAGE[out_fmt])
+    pre = np.empty(x.shape)
+    mag = np.empty(x.shape)
+    rc = _lib().oracle_layernorm(_ptr(out), out_fmt, _ptr(pre), _ptr(mag), _ptr(x), _ptr(gamma),
+                                 _ptr(beta), fmt, rows, hidden, eps, inv_scale)
+    _check(rc, "layernorm")
+    return out, pre, mag
+
+
+def quantize_static(x, fmt, inv_scale):
+    """E4M3 codes of a stored tensor under the static-scale epilogue."""
+    x = _c(x, STORAGE[fmt])
+    out = np.empty(x.shape, np.uint8)
+    rc = _lib().oracle_quantize_static(_ptr(out), _ptr(x), fmt, x.size, ctypes.c_float(inv_scale))
+    _check(rc, "quantize_static")
+    return out
 
 
 def glu_act(gate_up, fmt, act, out_fmt=None, inv_scale=1.0):

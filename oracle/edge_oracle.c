@@ -306,6 +306,61 @@ int oracle_add_rmsnorm(void* out, int out_fmt, double* pre, void* residual_out, 
 }
 
 /* ------------------------------------------------------------------ */
+/* LayerNorm ([FRT] siglip_layernorm_1read; Ba, Kiros and Hinton)      */
+/* ------------------------------------------------------------------ */
+
+/* y_i = (x_i - mu) / sqrt(var + eps) * gamma_i + beta_i with mu the row mean
+ * and var = mean((x - mu)^2) (biased).  gamma / beta may be absent (1 / 0).
+ * mag (nullable) receives the error scale of each output, the magnitudes of
+ * the terms whose roundings enter it: (|x_i| + |mu| + mean|x|) r |gamma_i| +
+ * |beta_i| (a float sum of the row errs in proportion to mean|x|). */
+int oracle_layernorm(void* out, int out_fmt, double* pre, double* mag, const void* x,
+                     const void* gamma, const void* beta, int f, int64_t rows, int64_t hidden,
+                     float eps, float inv_scale)
+{
+    if (!common_ok(out_fmt, f, rows, hidden, 0)) return 1;
+    double* xr = malloc(sizeof(double) * (size_t)(hidden + 1));
+    if (!xr) return 2;
+    for (int64_t t = 0; t < rows; ++t) {
+        double mu = 0.0, mean_abs = 0.0;
+        for (int64_t i = 0; i < hidden; ++i) {
+            xr[i] = load(x, f, t * hidden + i);
+            mu += xr[i];
+            mean_abs += fabs(xr[i]);
+        }
+        mu /= (double)hidden;
+        mean_abs /= (double)hidden;
+        double var = 0.0;
+        for (int64_t i = 0; i < hidden; ++i) var += (xr[i] - mu) * (xr[i] - mu);
+        var /= (double)hidden;
+        double r = 1.0 / sqrt(var + (double)eps);
+        for (int64_t i = 0; i < hidden; ++i) {
+            double g = gamma ? load(gamma, f, i) : 1.0;
+            double b = beta ? load(beta, f, i) : 0.0;
+            double y = (xr[i] - mu) * r * g + b;
+            store(out, out_fmt, t * hidden + i, emit(y, out_fmt, inv_scale));
+            if (pre) pre[t * hidden + i] = y;
+            if (mag) mag[t * hidden + i] = (fabs(xr[i]) + fabs(mu) + mean_abs) * r * fabs(g) + fabs(b);
+        }
+    }
+    free(xr);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Static FP8 quantization ([FRT] quantize_fp8_static)                 */
+/* ------------------------------------------------------------------ */
+
+/* out_i = E4M3(fl32(x_i) * inv_scale) with the epilogue's fp32 decision and
+ * saturation: the standalone form of the fused static-scale epilogue. */
+int oracle_quantize_static(void* out, const void* x, int f, int64_t n, float inv_scale)
+{
+    if (!fmt_ok(f) || f == OR_E4M3 || n < 0) return 1;
+    for (int64_t i = 0; i < n; ++i) store(out, OR_E4M3, i, emit(load(x, f, i), OR_E4M3, inv_scale));
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* Gated activations ([TEO] section 5.1; Shazeer GLU variants)         */
 /* ------------------------------------------------------------------ */
 

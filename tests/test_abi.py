@@ -90,6 +90,8 @@ def test_zero_rows_is_ok_and_launches_nothing(L):
     assert L.edge_rope(QO, KO, BF16, Q, K, BF16, 0, 8, 2, 128, 64, 0, POS, COS, SIN, 4096, 1.0,
                        None) == OK
     assert rms(L, rows=0) == OK
+    assert L.edge_layernorm(O, BF16, X, W, None, BF16, 0, 64, 1e-5, 1.0, None) == OK
+    assert L.edge_quantize_fp8(O, X, BF16, 0, 1.0, None) == OK
     assert add(L, rows=0) == OK
     assert glu(L, rows=0) == OK
     assert qk(L, T=0) == OK
@@ -139,6 +141,15 @@ def test_zero_rows_is_ok_and_launches_nothing(L):
                            4096, 1.0, None), SHAPE),
     (lambda L: L.edge_rope(Q + 2, KO, BF16, Q, K, BF16, 4, 8, 2, 128, 64, 0, POS, COS, SIN,
                            4096, 1.0, None), ALIAS),
+    (lambda L: L.edge_layernorm(O, BF16, None, W, W + 4096, BF16, 4, 64, 1e-5, 1.0, None), NULL),
+    (lambda L: L.edge_layernorm(O, BF16, X, W, W + 4096, BF16, 4, 64, -1.0, 1.0, None), VALUE),
+    (lambda L: L.edge_layernorm(X + 2, BF16, X, W, W + 4096, BF16, 4, 64, 1e-5, 1.0, None), ALIAS),
+    (lambda L: L.edge_layernorm(O, FP8, X, W, W + 4096, BF16, 4, 64, 1e-5, 0.0, None), VALUE),
+    (lambda L: L.edge_quantize_fp8(O, X, BF16, -1, 1.0, None), SHAPE),
+    (lambda L: L.edge_quantize_fp8(O, X, FP8, 16, 1.0, None), DTYPE),
+    (lambda L: L.edge_quantize_fp8(O, X, BF16, 16, float("nan"), None), VALUE),
+    (lambda L: L.edge_quantize_fp8(X + 8, X, BF16, 16, 1.0, None), ALIAS),
+    (lambda L: L.edge_quantize_fp8(O, X + 1, BF16, 16, 1.0, None), ALIGN),
     (lambda L: rms(L, hidden=2 ** 25, rows=1), UNSUP),
 ])
 def test_invalid_calls_are_rejected(L, call, status):

@@ -582,3 +582,68 @@ def test_qk_norm_rope_unrounded(name):
               ETA_NORM, lo=ref.q_lo, hi=ref.q_hi)
     check_out(name + " k", storage(ko.cpu()), ref.k_out, ref.k_pre, ref.k_mag, fmt, fmt,
               ETA_NORM, lo=ref.k_lo, hi=ref.k_hi)
+
+
+# ---------------------------------------------------------------- LayerNorm and static quantize
+
+LN_CASES = {
+    "siglip_bf16_h1152_T512": dict(dtype=torch.bfloat16, T=512, H=1152, affine=True),
+    "bf16_h2048_T3_noaffine": dict(dtype=torch.bfloat16, T=3, H=2048, affine=False),
+    "f32_h1024_T77": dict(dtype=torch.float32, T=77, H=1024, affine=True),
+    "f16_h37_generic": dict(dtype=torch.float16, T=40, H=37, affine=True),
+    "bf16_h1000_misaligned": dict(dtype=torch.bfloat16, T=9, H=1000, affine=True, misalign=1),
+    "bf16_h16384_T2": dict(dtype=torch.bfloat16, T=2, H=16384, affine=True),
+}
+
+
+def run_ln(c, fp8=False, inplace=False):
+    dtype, fmt = c["dtype"], TORCH_FMT[c["dtype"]]
+    rng = np.random.default_rng(31)
+    x = synth.to_dtype(synth.normal(0, 41, c["T"] * c["H"], 0.7, 2.0), dtype).view(c["T"], c["H"])
+    g = synth.to_dtype(synth.normal(0, 42, c["H"], 1.0, 0.1), dtype) if c["affine"] else None
+    b = synth.to_dtype(synth.normal(0, 43, c["H"], 0.0, 0.1), dtype) if c["affine"] else None
+    out_fmt = oracle.E4M3 if fp8 else fmt
+    inv = 448.0 / 5.0
+    ref, pre, mag = oracle.layernorm(storage(x), None if g is None else storage(g),
+                                     None if b is None else storage(b), fmt, 1e-5, out_fmt, inv)
+    mis = c.get("misalign", 0)
+    xd, gd, bd = dev(x, mis), dev(g, mis), dev(b, mis)
+    if inplace:
+        gout = Guarded(xd.shape, dtype)
+        gout.t.copy_(xd)
+        xd = gout.t
+    else:
+        gout = Guarded(xd.shape, torch.uint8 if fp8 else dtype, mis)
+    edge_ops.layernorm(xd, gd, bd, eps=1e-5, out=gout.t, fp8=fp8, inv_scale=inv)
+    torch.cuda.synchronize()
+    gout.check()
+    check_out("layernorm", storage(gout.t.cpu()), ref, pre, mag, fmt, out_fmt, ETA_NORM, inv)
+    del rng
+
+
+@pytest.mark.parametrize("name", list(LN_CASES))
+def test_layernorm(name):
+    run_ln(LN_CASES[name])
+
+
+@pytest.mark.parametrize("name", ["siglip_bf16_h1152_T512", "f16_h37_generic"])
+def test_layernorm_fp8_and_in_place(name):
+    run_ln(LN_CASES[name], fp8=True)
+    run_ln(LN_CASES[name], inplace=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("n,mis", [(1, 0), (8 * 1000 + 5, 0), (3 * 2 ** 20, 0), (77, 1)])
+def test_quantize_fp8(dtype, n, mis):
+    fmt = TORCH_FMT[dtype]
+    x = synth.to_dtype(synth.with_outliers(synth.normal(0, 51, n, 0.0, 1.0), 0, 52, 0.001, 20.0),
+                       dtype)
+    inv = float(np.float32(448.0 / 7.0))
+    ref = oracle.quantize_static(storage(x), fmt, inv)
+    xd = dev(x, mis)
+    g = Guarded((n,), torch.uint8, mis)
+    edge_ops.quantize_fp8(xd, inv, out=g.t)
+    torch.cuda.synchronize()
+    g.check()
+    # exact: the input is exact in fp32, so both sides take the same fp32 decision
+    assert np.array_equal(storage(g.t.cpu()), ref)

@@ -474,3 +474,53 @@ def test_rope_diagnostics_and_fp8():
     q8 = oracle.rope(storage(x), oracle.BF16, rho, oracle.ROTATE_HALF, pos, storage(cos),
                      storage(sin), out_fmt=oracle.E4M3, inv_scale=16.0)
     assert np.array_equal(q8, oracle.quantize(pre, 16.0))
+
+
+# ----------------------------------------------------------------- LayerNorm and static quantize
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("affine", [True, False])
+def test_layernorm_vs_torch_fp64(dtype, affine):
+    rng = np.random.default_rng(21)
+    x = torch.from_numpy(rng.standard_normal((6, 77)) * 3 + 1.5).to(dtype)
+    g = torch.from_numpy(1 + 0.1 * rng.standard_normal(77)).to(dtype) if affine else None
+    b = torch.from_numpy(0.1 * rng.standard_normal(77)).to(dtype) if affine else None
+    out, pre, mag = oracle.layernorm(storage(x), None if g is None else storage(g),
+                                     None if b is None else storage(b), FMT[dtype], 1e-5)
+    ref = F.layer_norm(torch.from_numpy(dec(x)), (77,),
+                       weight=None if g is None else torch.from_numpy(dec(g)),
+                       bias=None if b is None else torch.from_numpy(dec(b)),
+                       eps=E32(1e-5)).numpy()
+    np.testing.assert_allclose(pre, ref, rtol=1e-12, atol=1e-14)
+    assert np.array_equal(out, oracle.encode(pre, FMT[dtype]))
+    assert np.all(mag >= np.abs(pre) - 1e-12)
+
+
+def test_layernorm_closed_forms():
+    # no affine: each row has mean 0 and variance var/(var+eps); a constant row
+    # normalizes to beta; adding a constant to a row changes nothing
+    rng = np.random.default_rng(22)
+    # values on a 2^-10 grid, so that x + 64 is exact in fp32
+    x = torch.from_numpy(np.round(rng.standard_normal((4, 256)) * 1024) / 1024).float()
+    _, pre, _ = oracle.layernorm(storage(x), None, None, oracle.F32, 1e-3)
+    xv = x.double().numpy()
+    var = xv.var(axis=1)
+    np.testing.assert_allclose(pre.mean(axis=1), 0, atol=1e-13)
+    np.testing.assert_allclose(pre.var(axis=1), var / (var + E32(1e-3)), rtol=1e-12)
+    _, pre2, _ = oracle.layernorm(storage(x + 64.0), None, None, oracle.F32, 1e-3)
+    np.testing.assert_allclose(pre2, pre, atol=1e-11)
+    c = torch.full((1, 16), 2.5)
+    beta = torch.linspace(-1, 1, 16)
+    _, pc, _ = oracle.layernorm(storage(c), storage(torch.ones(16)), storage(beta), oracle.F32,
+                                1e-5)
+    np.testing.assert_allclose(pc[0], beta.double().numpy(), atol=1e-15)
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_quantize_static_vs_torch(dtype):
+    rng = np.random.default_rng(23)
+    x = torch.from_numpy(rng.standard_normal(5000) * 4).to(dtype)
+    inv = np.float32(448.0 / 9.0)
+    got = oracle.quantize_static(storage(x), FMT[dtype], float(inv))
+    ref = (x.float() * torch.tensor(inv)).clamp(-448, 448).to(torch.float8_e4m3fn)
+    assert np.array_equal(got, ref.view(torch.uint8).numpy())

@@ -201,6 +201,39 @@ edge_status edge_layernorm(void* out, edge_dtype out_dt, const void* x, const vo
 edge_status edge_quantize_fp8(void* out, const void* x, edge_dtype dt, int64_t n, float inv_scale,
                               void* stream);
 
+/*
+ * Fused QKV split + QK-norm + RoPE + KV-cache write (FlashRT
+ * "optimization-details": qkv_split_rope_kvcache; "thox-edge-ops v2",
+ * roadmap item 4: a KV write fused into the prologue).
+ *
+ * qkv:   [tokens, (q_heads + 2 kv_heads) head_dim] of dt.  Row t holds q_heads
+ *        query heads, then kv_heads key heads, then kv_heads value heads
+ *        (the output of a fused QKV projection).
+ * q_out: [tokens, q_heads, head_dim] of dt: the query heads after the prologue
+ *        of edge_qk_norm_rope (per-head RMSNorm when normalize = 1, rounded to
+ *        dt; the rotation of the first rotary_dim channels by cos/sin row
+ *        positions[t]).
+ * k_cache, v_cache: [num_slots, kv_heads, head_dim] of dt.  Row slots[t]
+ *        receives the key heads of token t after the same prologue, and the
+ *        value heads unchanged.  A token whose slot is negative or
+ *        >= num_slots writes no cache row, so the cache is never written out
+ *        of bounds; the other rows are left untouched.
+ * slots: [tokens] int64, device.  Caches and slots may be NULL when
+ *        kv_heads == 0 or num_slots == 0.
+ * Output dtype is dt (no FP8 epilogue).  Outputs must not overlap each other
+ * or any input.  This build has a vectorized path only: head_dim * size(dt) a
+ * power-of-two multiple of 16 up to 512 bytes, 16-byte aligned tensors, and a
+ * rotary width like edge_qk_norm_rope's vector path.  Other valid shapes
+ * return EDGE_ERR_UNSUPPORTED without launching.
+ */
+edge_status edge_qkv_rope_cache(void* q_out, void* k_cache, void* v_cache, const void* qkv,
+                                const void* wq, const void* wk, edge_dtype dt, int64_t tokens,
+                                int32_t q_heads, int32_t kv_heads, int32_t head_dim,
+                                int32_t rotary_dim, edge_rope_layout layout,
+                                const int64_t* positions, const float* cos, const float* sin,
+                                int64_t cache_len, const int64_t* slots, int64_t num_slots,
+                                float eps, int weight_offset, int normalize, void* stream);
+
 /* Flags of edge_qk_norm_rope_ex. */
 enum {
     /* Rotate the fp32 normalized value and round once after the rotation,

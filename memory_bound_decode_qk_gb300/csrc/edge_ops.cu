@@ -276,6 +276,90 @@ edge_status edge_add_rmsnorm(void* out, edge_dtype out_dt, const void* x, void* 
                       inv_scale, stream);
 }
 
+edge_status edge_qkv_rope_cache(void* q_out, void* k_cache, void* v_cache, const void* qkv,
+                                const void* wq, const void* wk, edge_dtype dt, int64_t tokens,
+                                int32_t q_heads, int32_t kv_heads, int32_t head_dim,
+                                int32_t rotary_dim, edge_rope_layout layout,
+                                const int64_t* positions, const float* cos, const float* sin,
+                                int64_t cache_len, const int64_t* slots, int64_t num_slots,
+                                float eps, int weight_offset, int normalize, void* stream) {
+    if (!act_dtype(dt)) return EDGE_ERR_DTYPE;
+    if (qkv == nullptr || q_out == nullptr) return EDGE_ERR_NULL;
+    const bool writes_cache = kv_heads > 0 && num_slots > 0;
+    if (writes_cache && (k_cache == nullptr || v_cache == nullptr || slots == nullptr)) {
+        return EDGE_ERR_NULL;
+    }
+    if (tokens < 0 || q_heads < 1 || kv_heads < 0 || head_dim < 1 || cache_len < 0 ||
+        num_slots < 0) {
+        return EDGE_ERR_SHAPE;
+    }
+    if (rotary_dim < 0 || rotary_dim > head_dim || (rotary_dim & 1)) return EDGE_ERR_SHAPE;
+    if (layout != EDGE_ROPE_ROTATE_HALF && layout != EDGE_ROPE_INTERLEAVED) return EDGE_ERR_VALUE;
+    if (!finite_nonneg(eps) || (weight_offset != 0 && weight_offset != 1) ||
+        (normalize != 0 && normalize != 1)) {
+        return EDGE_ERR_VALUE;
+    }
+    const bool may_rotate = rotary_dim > 0 && cache_len > 0;
+    if (may_rotate && (positions == nullptr || cos == nullptr || sin == nullptr)) {
+        return EDGE_ERR_NULL;
+    }
+    const int64_t es = esize(dt);
+    const int64_t heads_row = (int64_t)q_heads + 2 * (int64_t)kv_heads;
+    int64_t in_b = 0, q_b = 0, c_b = 0, cs_b = 0;
+    if (!checked_bytes(tokens, heads_row * head_dim, es, &in_b) ||
+        !checked_bytes(tokens, (int64_t)q_heads * head_dim, es, &q_b) ||
+        !checked_bytes(num_slots, (int64_t)kv_heads * head_dim, es, &c_b) ||
+        !checked_bytes(cache_len, rotary_dim / 2, 4, &cs_b)) {
+        return EDGE_ERR_SHAPE;
+    }
+    if (head_dim > edge::kMaxQKHeadDim) return EDGE_ERR_UNSUPPORTED;
+    if (tokens > edge::kMaxUnits / heads_row) return EDGE_ERR_UNSUPPORTED;
+    if (!aligned(qkv, es) || !aligned(q_out, es) || !aligned(k_cache, es) ||
+        !aligned(v_cache, es) || !aligned(wq, es) || !aligned(wk, es) || !aligned(positions, 8) ||
+        !aligned(slots, 8) || !aligned(cos, 4) || !aligned(sin, 4)) {
+        return EDGE_ERR_ALIGN;
+    }
+    const Span sq = span(q_out, q_b);
+    const Span sk = span(writes_cache ? k_cache : nullptr, c_b);
+    const Span sv = span(writes_cache ? v_cache : nullptr, c_b);
+    const Span ro[] = {span(qkv, in_b), span(wq, head_dim * es), span(wk, head_dim * es),
+                       span(may_rotate ? positions : nullptr, tokens * 8),
+                       span(may_rotate ? cos : nullptr, cs_b), span(may_rotate ? sin : nullptr, cs_b),
+                       span(writes_cache ? slots : nullptr, tokens * 8)};
+    if (overlap(sq, sk) || overlap(sq, sv) || overlap(sk, sv)) return EDGE_ERR_ALIAS;
+    for (const Span& r : ro) {
+        if (overlap(sq, r) || overlap(sk, r) || overlap(sv, r)) return EDGE_ERR_ALIAS;
+    }
+    if (tokens == 0) return EDGE_OK;
+    edge::QKVArgs a;
+    a.qkv = qkv;
+    a.q_out = q_out;
+    a.k_cache = writes_cache ? k_cache : nullptr;
+    a.v_cache = writes_cache ? v_cache : nullptr;
+    a.wq = wq;
+    a.wk = wk;
+    a.pos = may_rotate ? positions : nullptr;
+    a.cos = may_rotate ? cos : nullptr;
+    a.sin = may_rotate ? sin : nullptr;
+    a.slots = writes_cache ? slots : nullptr;
+    a.tokens = tokens;
+    a.cache_len = cache_len;
+    a.num_slots = writes_cache ? num_slots : 0;
+    a.q_heads = q_heads;
+    a.kv_heads = kv_heads;
+    a.head_dim = head_dim;
+    a.rotary_dim = rotary_dim;
+    a.layout = (int)layout;
+    a.dt = (int)dt;
+    a.normalize = normalize;
+    a.weight_offset = weight_offset;
+    a.eps = eps;
+    bool handled = false;
+    cudaError_t e = edge::launch_qkv_cache(a, static_cast<cudaStream_t>(stream), &handled);
+    if (e == cudaSuccess && !handled) return EDGE_ERR_UNSUPPORTED;
+    return finish(e);
+}
+
 edge_status edge_layernorm(void* out, edge_dtype out_dt, const void* x, const void* gamma,
                            const void* beta, edge_dtype dt, int64_t rows, int64_t hidden,
                            float eps, float inv_scale, void* stream) {

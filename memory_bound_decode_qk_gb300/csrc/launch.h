@@ -61,6 +61,25 @@ cudaError_t launch_qk(const QKArgs& a, cudaStream_t s);
 cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s);
 cudaError_t launch_glu(const GluArgs& a, cudaStream_t s);
 
+struct QKVArgs {
+    const void* qkv;
+    void* q_out;
+    void* k_cache;
+    void* v_cache;
+    const void* wq;          // nullable
+    const void* wk;          // nullable
+    const int64_t* pos;
+    const float* cos;
+    const float* sin;
+    const int64_t* slots;
+    int64_t tokens, cache_len, num_slots;
+    int q_heads, kv_heads, head_dim, rotary_dim, layout, dt;
+    int normalize, weight_offset;
+    float eps;
+};
+// *handled is false when the geometry or alignment has no vector path.
+cudaError_t launch_qkv_cache(const QKVArgs& a, cudaStream_t s, bool* handled);
+
 struct QuantArgs {
     const void* x;
     void* out;

@@ -68,6 +68,165 @@ __device__ __forceinline__ Unit locate(const QKP& p, uint32_t u) {
 }
 
 
+// ---------------------------------------------------------------- shared head math
+
+// Cache entries a lane needs: rotate-half lanes hold N consecutive channels of
+// one half (N entries); interleaved lanes hold N/2 pairs (N/2 entries).
+template <typename T, int LAYOUT>
+struct CacheRegs {
+    static constexpr int N = vec_elems<T>();
+    static constexpr int kCount = LAYOUT == kInterleaved ? N / 2 : N;
+    float c[kCount], s[kCount];
+};
+
+// Role of a lane's vector in the rotation: 0 none, 1 first member, 2 second.
+template <typename T, int LAYOUT>
+__device__ __forceinline__ int rotary_role(const QKP& p, int sub) {
+    constexpr int N = vec_elems<T>();
+    const int e0 = sub * N;
+    if constexpr (LAYOUT == kInterleaved) {
+        return e0 < p.rot ? 1 : 0;
+    } else {
+        return e0 < p.half ? 1 : (e0 < p.rot ? 2 : 0);
+    }
+}
+
+// Load this lane's cos/sin entries of cache row `pos` (role != 0 only).
+template <typename T, int LAYOUT>
+__device__ __forceinline__ void load_cache(const QKP& p, int64_t pos, int sub, int role,
+                                           CacheRegs<T, LAYOUT>& cr) {
+    constexpr int N = vec_elems<T>();
+    const int e0 = sub * N;
+    if constexpr (LAYOUT == kInterleaved) {
+        const float* crow = p.cs + pos * p.half + e0 / 2;
+        const float* srow = p.sn + pos * p.half + e0 / 2;
+        if constexpr (N == 8) {
+            float4 c4 = __ldg(reinterpret_cast<const float4*>(crow));
+            float4 s4 = __ldg(reinterpret_cast<const float4*>(srow));
+            cr.c[0] = c4.x; cr.c[1] = c4.y; cr.c[2] = c4.z; cr.c[3] = c4.w;
+            cr.s[0] = s4.x; cr.s[1] = s4.y; cr.s[2] = s4.z; cr.s[3] = s4.w;
+        } else {
+            float2 c2 = __ldg(reinterpret_cast<const float2*>(crow));
+            float2 s2 = __ldg(reinterpret_cast<const float2*>(srow));
+            cr.c[0] = c2.x; cr.c[1] = c2.y;
+            cr.s[0] = s2.x; cr.s[1] = s2.y;
+        }
+    } else {
+        const int j0 = role == 1 ? e0 : e0 - p.half;
+        const float4* c4 = reinterpret_cast<const float4*>(p.cs + pos * p.half + j0);
+        const float4* s4 = reinterpret_cast<const float4*>(p.sn + pos * p.half + j0);
+#pragma unroll
+        for (int v = 0; v < N / 4; ++v) {
+            float4 cc = __ldg(c4 + v), sv = __ldg(s4 + v);
+            cr.c[4 * v] = cc.x; cr.c[4 * v + 1] = cc.y; cr.c[4 * v + 2] = cc.z; cr.c[4 * v + 3] = cc.w;
+            cr.s[4 * v] = sv.x; cr.s[4 * v + 1] = sv.y; cr.s[4 * v + 2] = sv.z; cr.s[4 * v + 3] = sv.w;
+        }
+    }
+}
+
+// Normalize, round to the dtype, rotate and store one head held as one
+// 16-byte vector per lane of an LPH-lane group.  w holds w + delta.  All 32
+// lanes of the warp call this together (the rotate-half partner comes over a
+// warp shuffle); inactive groups carry zeros and store nothing.  `role` is
+// this lane's rotation role for this head's token (0 when it does not rotate).
+//  copy: pass the head through unnormalized and unrotated (the v heads of
+//  the fused QKV op); the lane group still joins the warp-wide reduction.
+template <typename T, bool FP8, int LPH, int LAYOUT>
+__device__ __forceinline__ void qk_core(const QKP& p, char* dst, bool active, int lane, int sub,
+                                        const uint4& raw, const float (&w)[vec_elems<T>()], int role,
+                                        const CacheRegs<T, LAYOUT>& cr, bool copy = false) {
+    constexpr int N = vec_elems<T>();
+    float x[N];
+    unpack_vec<T, N>(raw, x);
+    // normalized value n (fp32); without normalization n = x
+    float n[N];
+    if (p.mode & kModeNorm) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+        ss = group_sum<LPH>(ss);
+        const float r = inv_rms(ss, p.invD, p.eps);
+#pragma unroll
+        for (int i = 0; i < N; ++i) n[i] = copy ? x[i] : __fmul_rn(__fmul_rn(x[i], r), w[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) n[i] = x[i];
+    }
+    // m: n rounded to the activation dtype.  The rotation consumes m, or n
+    // itself in the unrounded mode; channels that do not rotate emit m.
+    const bool unrounded = (p.mode & kModeUnrounded) != 0;
+    float m[N], src[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        m[i] = round_to<T>(n[i]);
+        src[i] = unrounded ? n[i] : m[i];
+    }
+
+    float y[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) y[i] = m[i];
+
+    if constexpr (LAYOUT == kInterleaved) {
+        if (role != 0) {
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                const float a = src[2 * i], b = src[2 * i + 1];
+                y[2 * i] = __fmaf_rn(a, cr.c[i], -__fmul_rn(b, cr.s[i]));
+                y[2 * i + 1] = __fmaf_rn(b, cr.c[i], __fmul_rn(a, cr.s[i]));
+            }
+        }
+    } else {
+        // rotate-half: channel e pairs with e + half; the partner vector is
+        // held by the lane half/N positions away in the same lane group
+        const int hv = p.half / N;
+        const int from = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
+        float pm[N];
+        if (unrounded) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) pm[i] = __shfl_sync(0xffffffffu, src[i], from);
+        } else {
+            const uint4 mine = pack_vec<T, N>(m);  // exact: m is already rounded to T
+            uint4 other;
+            other.x = __shfl_sync(0xffffffffu, mine.x, from);
+            other.y = __shfl_sync(0xffffffffu, mine.y, from);
+            other.z = __shfl_sync(0xffffffffu, mine.z, from);
+            other.w = __shfl_sync(0xffffffffu, mine.w, from);
+            unpack_vec<T, N>(other, pm);
+        }
+        if (role == 1) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(src[i], cr.c[i], -__fmul_rn(pm[i], cr.s[i]));
+        } else if (role == 2) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(src[i], cr.c[i], __fmul_rn(pm[i], cr.s[i]));
+        }
+    }
+
+    if (active) {
+        if constexpr (FP8) {
+            auto q8 = quantize_vec<N>(y, p.inv);
+            reinterpret_cast<decltype(q8)*>(dst)[sub] = q8;
+        } else {
+            reinterpret_cast<uint4*>(dst)[sub] = pack_vec<T, N>(y);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void weights_plus_delta(const QKP& p, const char* wptr, int sub,
+                                                   float (&w)[vec_elems<T>()]) {
+    constexpr int N = vec_elems<T>();
+    if (wptr != nullptr) {
+        uint4 wr = __ldg(reinterpret_cast<const uint4*>(wptr) + sub);
+        unpack_vec<T, N>(wr, w);
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = __fadd_rn(w[i], p.delta);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = 1.0f;
+    }
+}
+
 // Threads-per-head path for many heads (qk_quad.cu).  *handled is false when
 // the geometry is outside its instantiations; the caller then takes the
 // lane-group path.

@@ -1,0 +1,188 @@
+// qkv_cache.cu -- fused QKV split + QK-norm + RoPE + KV-cache write (sm_103a).
+//
+// What it computes (FlashRT "optimization-details": qkv_split_rope_kvcache;
+// "thox-edge-ops v2", roadmap item 4, a KV write fused into the prologue).
+// Row t of the fused projection output qkv [T, (Hq + 2 Hk) D] holds Hq query
+// heads, Hk key heads and Hk value heads.
+//   - Query heads get the prologue (optional per-head RMSNorm, rounded to the
+//     dtype, rotary embedding of the first rotary_dim channels) into
+//     q_out[t].
+//   - Key heads get the same into k_cache[slots[t]].
+//   - Value heads are copied unchanged into v_cache[slots[t]].
+// Caches are [num_slots, Hk, D].  A token whose slot is outside [0, num_slots)
+// writes no cache row, so it cannot write out of bounds; its query still goes
+// to q_out.
+//
+// GB300 design: the lane-group layout of the decode-width prologue.  A head is
+// one 16-byte vector per lane of an LPH-lane group, and a one-shot grid puts
+// every head in flight, the regime of decode widths.  Units are token-major
+// over the Hq + 2 Hk heads of a row.  A v head rides the same code with no
+// norm and no rotation, so a warp never diverges around the shuffles.
+#include "qk_common.cuh"
+
+namespace edge {
+namespace {
+
+struct QKVP {
+    QKP p;                 // q_heads, k_heads, D, rot, cache, eps, weights, q output
+    char* kc;              // k_cache
+    char* vc;              // v_cache
+    const int64_t* slots;
+    int64_t num_slots;
+    int64_t row_bytes;     // bytes of one qkv row
+    FastDiv per_token;     // Hq + 2 Hk
+};
+
+template <typename T, int LPH, int LAYOUT>
+__global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
+    constexpr int N = vec_elems<T>();
+    constexpr int HPW = 32 / LPH;
+    const QKP& p = a.p;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (LPH - 1);
+    const int slot_in_warp = lane / LPH;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int hb = p.D * (int)sizeof(T);
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (uint32_t base = warp * HPW; base < p.units; base += nwarps * HPW) {
+        const uint32_t u = base + slot_in_warp;
+        const bool active = u < p.units;
+        const uint32_t t = fast_div(active ? u : base, a.per_token);
+        const int h = (int)((active ? u : base) - t * a.per_token.d);
+        const char* src = p.q + (int64_t)t * a.row_bytes + (int64_t)h * hb;
+        const bool isq = h < p.q_heads;
+        const bool isv = h >= p.q_heads + p.k_heads;
+        const int j = isq ? h : (isv ? h - p.q_heads - p.k_heads : h - p.q_heads);
+
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        int64_t pos = -1, slot = -1;
+        if (active) {
+            raw = __ldcs(reinterpret_cast<const uint4*>(src) + sub);
+            if (p.rot > 0 && !isv) pos = __ldg(p.pos + t);
+            if (!isq) slot = __ldg(a.slots + t);
+        }
+        char* dst = nullptr;
+        if (isq) {
+            dst = p.qo + ((int64_t)t * p.q_heads + j) * hb;
+        } else if (slot >= 0 && slot < a.num_slots) {
+            dst = (isv ? a.vc : a.kc) + (slot * p.k_heads + j) * hb;
+        }
+        float w[N];
+        weights_plus_delta<T>(p, isq ? p.wq : p.wk, sub, w);
+        const bool rot = active && !isv && pos >= 0 && pos < p.cache_len;
+        const int role = rot ? rotary_role<T, LAYOUT>(p, sub) : 0;
+        CacheRegs<T, LAYOUT> cr;
+        if (role != 0) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
+        qk_core<T, false, LPH, LAYOUT>(p, dst, active && dst != nullptr, lane, sub, raw, w, role,
+                                       cr, isv);
+    }
+}
+
+template <typename T>
+cudaError_t launch_typed(const QKVArgs& a, QKVP& k, cudaStream_t s, bool* handled) {
+    constexpr int N = vec_elems<T>();
+    *handled = false;
+    const int D = a.head_dim;
+    const int nvec = (D * (int)sizeof(T)) % 16 == 0 ? D * (int)sizeof(T) / 16 : 0;
+    auto aligned = [](const void* ptr, uintptr_t n) {
+        return ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) % n) == 0;
+    };
+    bool vec = nvec > 0 && nvec <= 32 && (nvec & (nvec - 1)) == 0;
+    vec = vec && aligned(a.qkv, 16) && aligned(a.wq, 16) && aligned(a.wk, 16) &&
+          aligned(a.q_out, 16) && aligned(a.k_cache, 16) && aligned(a.v_cache, 16);
+    if (k.p.rot > 0) {
+        if (a.layout == kInterleaved) {
+            vec = vec && k.p.rot % N == 0 && aligned(a.cos, 8 * (N / 4)) && aligned(a.sin, 8 * (N / 4));
+        } else {
+            vec = vec && (k.p.rot / 2) % N == 0 && aligned(a.cos, 16) && aligned(a.sin, 16);
+        }
+    }
+    if (!vec) return cudaSuccess;
+    *handled = true;
+    const int lph = nvec;
+    const int hpw = 32 / lph;
+    const int threads = 256;
+    const int64_t per_block = (int64_t)(threads / 32) * hpw;
+    int64_t blocks = ((int64_t)k.p.units + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)sm_count() * (2048 / threads) * 64;
+    if (blocks > cap) blocks = cap;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+#define EDGE_QKV_CASE(L)                                                                  \
+    case L:                                                                                \
+        return a.layout == kInterleaved ? cudaLaunchKernelEx(&cfg, qkv_vec_kernel<T, L, kInterleaved>, k) \
+                                        : cudaLaunchKernelEx(&cfg, qkv_vec_kernel<T, L, kRotateHalf>, k);
+    switch (lph) {
+        EDGE_QKV_CASE(1)
+        EDGE_QKV_CASE(2)
+        EDGE_QKV_CASE(4)
+        EDGE_QKV_CASE(8)
+        EDGE_QKV_CASE(16)
+        EDGE_QKV_CASE(32)
+        default: break;
+    }
+#undef EDGE_QKV_CASE
+    *handled = false;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_qkv_cache(const QKVArgs& a, cudaStream_t s, bool* handled) {
+    QKVP k;
+    QKP& p = k.p;
+    const int es = a.dt == kF32 ? 4 : 2;
+    const bool may_rotate = a.rotary_dim > 0 && a.cache_len > 0 && a.pos && a.cos && a.sin;
+    p.q = static_cast<const char*>(a.qkv);
+    p.k = nullptr;
+    p.qo = static_cast<char*>(a.q_out);
+    p.ko = nullptr;
+    p.wq = static_cast<const char*>(a.wq);
+    p.wk = static_cast<const char*>(a.wk);
+    p.pos = a.pos;
+    p.cs = a.cos;
+    p.sn = a.sin;
+    p.cache_len = may_rotate ? a.cache_len : 0;
+    p.tokens = a.tokens;
+    p.units = (uint32_t)(a.tokens * (a.q_heads + 2 * a.kv_heads));
+    p.heads = make_fastdiv((uint32_t)(a.q_heads + 2 * a.kv_heads));
+    p.qdiv = make_fastdiv((uint32_t)a.q_heads);
+    p.kdiv = make_fastdiv((uint32_t)(a.kv_heads > 0 ? a.kv_heads : 1));
+    p.qrows = (uint32_t)(a.tokens * a.q_heads);
+    p.q_heads = a.q_heads;
+    p.k_heads = a.kv_heads;
+    p.D = a.head_dim;
+    p.rot = may_rotate ? a.rotary_dim : 0;
+    p.half = p.rot / 2;
+    p.in_bytes = es;
+    p.out_bytes = es;
+    p.eps = a.eps;
+    p.delta = (float)a.weight_offset;
+    p.inv = 1.0f;
+    p.invD = 1.0f / (float)a.head_dim;
+    p.mode = a.normalize ? kModeNorm : 0;
+    k.kc = static_cast<char*>(a.k_cache);
+    k.vc = static_cast<char*>(a.v_cache);
+    k.slots = a.slots;
+    k.num_slots = a.num_slots;
+    k.row_bytes = (int64_t)(a.q_heads + 2 * a.kv_heads) * a.head_dim * es;
+    k.per_token = p.heads;
+    switch (a.dt) {
+        case kF32: return launch_typed<float>(a, k, s, handled);
+        case kF16: return launch_typed<__half>(a, k, s, handled);
+        default: return launch_typed<__nv_bfloat16>(a, k, s, handled);
+    }
+}
+
+}  // namespace edge

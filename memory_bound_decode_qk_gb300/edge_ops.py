@@ -26,6 +26,7 @@ STATUS = {
 }
 EXPORTS = ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope",
            "edge_qk_norm_rope_ex", "edge_rope", "edge_layernorm", "edge_quantize_fp8",
+           "edge_qkv_rope_cache",
            "edge_status_str", "edge_last_cuda_error", "edge_version")
 QK_ROTATE_UNROUNDED = 1
 
@@ -72,8 +73,11 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
     L.edge_rope.argtypes = [P, P, I, P, P, I, I64, I32, I32, I32, I32, I, P, P, P, I64, F, P]
     L.edge_layernorm.argtypes = [P, I, P, P, P, I, I64, I64, F, F, P]
     L.edge_quantize_fp8.argtypes = [P, P, I, I64, F, P]
+    L.edge_qkv_rope_cache.argtypes = [P, P, P, P, P, P, I, I64, I32, I32, I32, I32, I, P, P, P,
+                                      I64, P, I64, F, I, I, P]
     for name in ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope",
-                 "edge_qk_norm_rope_ex", "edge_rope", "edge_layernorm", "edge_quantize_fp8"):
+                 "edge_qk_norm_rope_ex", "edge_rope", "edge_layernorm", "edge_quantize_fp8",
+                 "edge_qkv_rope_cache"):
         getattr(L, name).restype = I
     L.edge_status_str.argtypes = [I]
     L.edge_status_str.restype = ctypes.c_char_p
@@ -170,6 +174,31 @@ def quantize_fp8(x, inv_scale, *, out=None, stream=None):
     _check(lib().edge_quantize_fp8(_ptr(out), _ptr(x), _dt(x), x.numel(), inv_scale,
                                    _stream(stream)), "edge_quantize_fp8")
     return out
+
+
+def qkv_rope_cache(qkv, q_heads, kv_heads, wq, wk, positions, cos, sin, slots, k_cache, v_cache,
+                   *, rotary_dim=None, layout=ROTATE_HALF, eps=1e-6, weight_offset=0,
+                   normalize=True, q_out=None, cache_len=None, stream=None):
+    """Fused QKV split + prologue + KV-cache write.  qkv: [T, (Hq + 2 Hk) D];
+    k_cache, v_cache: [S, Hk, D] (written at rows slots[t]).  Returns q_out."""
+    _need_contig(qkv, wq, wk, positions, cos, sin, slots, k_cache, v_cache, q_out)
+    T = qkv.shape[0]
+    D = qkv.shape[-1] // (q_heads + 2 * kv_heads)
+    if rotary_dim is None:
+        rotary_dim = D if cos is None else 2 * cos.shape[-1]
+    if cache_len is None:
+        cache_len = 0 if cos is None else cos.shape[0]
+    if isinstance(layout, str):
+        layout = {"rotate_half": ROTATE_HALF, "interleaved": INTERLEAVED}[layout]
+    if q_out is None:
+        q_out = torch.empty((T, q_heads, D), dtype=qkv.dtype, device=qkv.device)
+    S = k_cache.shape[0] if k_cache is not None else 0
+    _check(lib().edge_qkv_rope_cache(_ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(qkv),
+                                     _ptr(wq), _ptr(wk), _dt(qkv), T, q_heads, kv_heads, D,
+                                     rotary_dim, layout, _ptr(positions), _ptr(cos), _ptr(sin),
+                                     cache_len, _ptr(slots), S, eps, weight_offset,
+                                     1 if normalize else 0, _stream(stream)), "edge_qkv_rope_cache")
+    return q_out
 
 
 def glu_act(gate_up, act=SILU, *, out=None, fp8=False, inv_scale=1.0, stream=None):

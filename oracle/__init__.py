@@ -70,9 +70,12 @@ def _lib():
                                           I, I, I, I, P, P, P, I64, F, I, F, D, I]
         L.oracle_layernorm.argtypes = [P, I, P, P, P, P, P, I, I64, I64, F, F]
         L.oracle_quantize_static.argtypes = [P, P, I, I64, F]
+        L.oracle_qkv_rope_cache.argtypes = [P] * 14 + [I, I64, I, I, I, I, I, P, P, P, I64, P, I64,
+                                                         F, I, I, D]
         L.oracle_set_rotation_scale.argtypes = [D]
         for name in ("oracle_rmsnorm", "oracle_add_rmsnorm", "oracle_glu_act", "oracle_rope",
                      "oracle_qk_norm_rope", "oracle_layernorm", "oracle_quantize_static",
+                     "oracle_qkv_rope_cache",
                      "oracle_version"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
@@ -272,6 +275,41 @@ def qk_norm_rope(q, k, wq, wk, fmt, rotary_dim, layout, positions, cos, sin, eps
         _ptr(wq), _ptr(wk), fmt, T, Hq, Hk, D, rotary_dim, layout, _ptr(positions), _ptr(cos),
         _ptr(sin), cache_len, eps, weight_offset, inv_scale, eta, 1 if unrounded else 0)
     _check(rc, "qk_norm_rope")
+    return res
+
+
+def qkv_rope_cache(qkv, wq, wk, fmt, q_heads, kv_heads, rotary_dim, layout, positions, cos, sin,
+                   slots, k_cache, v_cache, eps, weight_offset=0, normalize=True,
+                   eta=2.0 ** -20, cache_len=None):
+    """Fused QKV split + prologue + KV-cache write.  qkv: [T, (Hq + 2 Hk) D]
+    storage; k_cache, v_cache: [S, Hk, D] storage, updated in copies (rows
+    whose slot is invalid keep their contents).  Returns a QKResult with
+    q_out, k_cache, v_cache and the diagnostics of q (q_*) and of the cache
+    rows (k_*)."""
+    qkv = _c(qkv, STORAGE[fmt])
+    T = qkv.shape[0]
+    D = qkv.shape[1] // (q_heads + 2 * kv_heads)
+    positions = _c(np.asarray(positions, np.int64))
+    slots = _c(np.asarray(slots, np.int64))
+    cos = _c(cos, np.float32)
+    sin = _c(sin, np.float32)
+    if cache_len is None:
+        cache_len = 0 if cos is None else cos.shape[0]
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    S = kc.shape[0]
+    res = QKResult(q_out=np.empty((T, q_heads, D), STORAGE[fmt]), k_cache=kc, v_cache=vc,
+                   q_pre=np.empty((T, q_heads, D)), q_lo=np.empty((T, q_heads, D)),
+                   q_hi=np.empty((T, q_heads, D)), q_mag=np.empty((T, q_heads, D)),
+                   k_pre=np.full(kc.shape, np.nan), k_lo=np.full(kc.shape, np.nan),
+                   k_hi=np.full(kc.shape, np.nan), k_mag=np.full(kc.shape, np.nan))
+    rc = _lib().oracle_qkv_rope_cache(
+        _ptr(res.q_out), _ptr(kc), _ptr(vc), _ptr(res.q_pre), _ptr(res.q_lo), _ptr(res.q_hi),
+        _ptr(res.q_mag), _ptr(res.k_pre), _ptr(res.k_lo), _ptr(res.k_hi), _ptr(res.k_mag),
+        _ptr(qkv), _ptr(_c(wq, STORAGE[fmt])), _ptr(_c(wk, STORAGE[fmt])), fmt, T, q_heads,
+        kv_heads, D, rotary_dim, layout, _ptr(positions), _ptr(cos), _ptr(sin), cache_len,
+        _ptr(slots), S, eps, weight_offset, 1 if normalize else 0, eta)
+    _check(rc, "qkv_rope_cache")
     return res
 
 

@@ -508,20 +508,27 @@ static int near_tie(double v, int f, double eta, double* other)
     return 1;
 }
 
-static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, const double* w, int f,
-                     int64_t t, int heads, int D, int rho, int layout, int rot, int64_t p,
-                     const float* cs, const float* sn, float eps, int delta, float inv_scale,
-                     double eta, int unrounded, double* xr, double* n, double* m,
-                     double* malt, int* tie, double* y, double* ylo, double* yhi)
+/* `heads` heads of D elements read from x at element offset x_off and
+ * written to out (and the diagnostics) at element offset out_off; without
+ * `normalize` the head passes through unnormalized (standalone rotation, or
+ * the value heads of the fused QKV op). */
+static void qk_heads(void* out, int out_fmt, qk_diag dg, const void* x, int64_t x_off,
+                     int64_t out_off, const double* w, int f, int heads, int D, int rho,
+                     int layout, int rot, int64_t p, const float* cs, const float* sn, float eps,
+                     int delta, float inv_scale, double eta, int unrounded, int normalize,
+                     double* xr, double* n, double* m, double* malt, int* tie, double* y,
+                     double* ylo, double* yhi)
 {
     int half = rho / 2;
     for (int h = 0; h < heads; ++h) {
-        int64_t base = ((int64_t)t * heads + h) * D;
-        for (int i = 0; i < D; ++i) xr[i] = load(x, f, base + i);
+        int64_t xb = x_off + (int64_t)h * D;
+        int64_t base = out_off + (int64_t)h * D;
+        for (int i = 0; i < D; ++i) xr[i] = load(x, f, xb + i);
         /* per-head RMSNorm with the head's own weight, then rounding to the
          * input dtype before the rotation ([TEO] section 5.4; [NIN]
          * "Implementation": the rotation consumes the rounded value). */
-        rms_row(xr, w, delta, D, (double)eps, n);
+        if (normalize) rms_row(xr, w, delta, D, (double)eps, n);
+        else for (int i = 0; i < D; ++i) n[i] = xr[i];
         for (int i = 0; i < D; ++i) {
             m[i] = oracle_round(n[i], f);
             malt[i] = m[i];
@@ -635,14 +642,71 @@ int oracle_qk_norm_rope(void* q_out, void* k_out, int out_fmt, double* q_pre, do
     for (int64_t t = 0; t < tokens; ++t) {
         int64_t p = positions ? positions[t] : -1;
         int rot = rotary_dim > 0 && in_cache(p, cache_len);
-        qk_heads(q_out, out_fmt, dq, q, wq ? wqr : NULL, f, t, q_heads, head_dim, rotary_dim,
+        const int64_t qo = t * q_heads * (int64_t)head_dim, ko = t * k_heads * (int64_t)head_dim;
+        qk_heads(q_out, out_fmt, dq, q, qo, qo, wq ? wqr : NULL, f, q_heads, head_dim, rotary_dim,
                  layout, rot, p, cos_cache, sin_cache, eps, weight_offset, inv_scale, eta,
-                 unrounded, buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd,
+                 unrounded, 1, buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd,
                  buf + 5 * nd, buf + 6 * nd);
-        qk_heads(k_out, out_fmt, dk, k, wk ? wkr : NULL, f, t, k_heads, head_dim, rotary_dim,
+        qk_heads(k_out, out_fmt, dk, k, ko, ko, wk ? wkr : NULL, f, k_heads, head_dim, rotary_dim,
                  layout, rot, p, cos_cache, sin_cache, eps, weight_offset, inv_scale, eta,
-                 unrounded, buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd,
+                 unrounded, 1, buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd,
                  buf + 5 * nd, buf + 6 * nd);
+    }
+    free(wqr); free(wkr); free(buf); free(tie);
+    return 0;
+}
+
+/* Fused QKV split + QK-norm + RoPE + KV-cache write ([FRT]
+ * qkv_split_rope_kvcache; [TEO] roadmap item 4).  Row t of qkv [T,
+ * (Hq + 2 Hk) D] holds Hq query, Hk key and Hk value heads.  Query heads get
+ * the prologue (per-head RMSNorm if `normalize`, rounding to the dtype, the
+ * rotation) into q_out[t]; key heads the same into k_cache[slots[t]]; value
+ * heads are copied into v_cache[slots[t]].  Caches are [num_slots, Hk, D]; a
+ * slot outside [0, num_slots) writes no cache row (the other rows keep their
+ * contents).  Diagnostics are laid out like q_out and k_cache. */
+int oracle_qkv_rope_cache(void* q_out, void* k_cache, void* v_cache, double* q_pre, double* q_lo,
+                          double* q_hi, double* q_mag, double* k_pre, double* k_lo, double* k_hi,
+                          double* k_mag, const void* qkv, const void* wq, const void* wk, int f,
+                          int64_t tokens, int q_heads, int kv_heads, int head_dim, int rotary_dim,
+                          int layout, const int64_t* positions, const float* cos_cache,
+                          const float* sin_cache, int64_t cache_len, const int64_t* slots,
+                          int64_t num_slots, float eps, int weight_offset, int normalize,
+                          double eta)
+{
+    if (!common_ok(f, f, tokens, head_dim, weight_offset)) return 1;
+    if (q_heads < 1 || kv_heads < 0 || head_dim <= 0 || num_slots < 0) return 1;
+    if (rotary_dim < 0 || rotary_dim > head_dim || (rotary_dim & 1)) return 1;
+    if (layout != OR_ROTATE_HALF && layout != OR_INTERLEAVED) return 1;
+    size_t nd = (size_t)head_dim + 1;
+    double* wqr = malloc(sizeof(double) * nd);
+    double* wkr = malloc(sizeof(double) * nd);
+    double* buf = malloc(sizeof(double) * nd * 8);
+    int* tie = malloc(sizeof(int) * nd);
+    if (!wqr || !wkr || !buf || !tie) { free(wqr); free(wkr); free(buf); free(tie); return 2; }
+    for (int i = 0; i < head_dim; ++i) {
+        wqr[i] = wq ? load(wq, f, i) : 1.0;
+        wkr[i] = wk ? load(wk, f, i) : 1.0;
+    }
+    const int64_t row = (int64_t)(q_heads + 2 * kv_heads) * head_dim;
+    qk_diag dq = {q_pre, q_lo, q_hi, q_mag}, dk = {k_pre, k_lo, k_hi, k_mag}, dv = {0, 0, 0, 0};
+    for (int64_t t = 0; t < tokens; ++t) {
+        int64_t p = positions ? positions[t] : -1;
+        int rot = rotary_dim > 0 && in_cache(p, cache_len);
+        qk_heads(q_out, f, dq, qkv, t * row, t * q_heads * (int64_t)head_dim, wq ? wqr : NULL, f,
+                 q_heads, head_dim, rotary_dim, layout, rot, p, cos_cache, sin_cache, eps,
+                 weight_offset, 1.0f, eta, 0, normalize, buf, buf + nd, buf + 2 * nd,
+                 buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd, buf + 6 * nd);
+        int64_t sl = slots ? slots[t] : -1;
+        if (kv_heads == 0 || sl < 0 || sl >= num_slots) continue;
+        const int64_t co = sl * kv_heads * (int64_t)head_dim;
+        qk_heads(k_cache, f, dk, qkv, t * row + (int64_t)q_heads * head_dim, co,
+                 wk ? wkr : NULL, f, kv_heads, head_dim, rotary_dim, layout, rot, p, cos_cache,
+                 sin_cache, eps, weight_offset, 1.0f, eta, 0, normalize, buf, buf + nd,
+                 buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd, buf + 6 * nd);
+        qk_heads(v_cache, f, dv, qkv, t * row + (int64_t)(q_heads + kv_heads) * head_dim, co,
+                 NULL, f, kv_heads, head_dim, 0, layout, 0, -1, NULL, NULL, eps, 0, 1.0f, eta, 0,
+                 0, buf, buf + nd, buf + 2 * nd, buf + 3 * nd, tie, buf + 4 * nd, buf + 5 * nd,
+                 buf + 6 * nd);
     }
     free(wqr); free(wkr); free(buf); free(tie);
     return 0;

@@ -150,6 +150,14 @@ def test_zero_rows_is_ok_and_launches_nothing(L):
     (lambda L: L.edge_quantize_fp8(O, X, BF16, 16, float("nan"), None), VALUE),
     (lambda L: L.edge_quantize_fp8(X + 8, X, BF16, 16, 1.0, None), ALIAS),
     (lambda L: L.edge_quantize_fp8(O, X + 1, BF16, 16, 1.0, None), ALIGN),
+    (lambda L: L.edge_qkv_rope_cache(QO, KO, KO + 65536, Q, WQ, WK, BF16, 4, 8, 2, 128, 64, 0,
+                                     POS, COS, SIN, 4096, None, 16, 1e-6, 0, 1, None), NULL),
+    (lambda L: L.edge_qkv_rope_cache(QO, KO, KO, Q, WQ, WK, BF16, 4, 8, 2, 128, 64, 0, POS, COS,
+                                     SIN, 4096, POS + 4096, 16, 1e-6, 0, 1, None), ALIAS),
+    (lambda L: L.edge_qkv_rope_cache(QO, KO, KO + 65536, Q, WQ, WK, BF16, 4, 8, 2, 128, 64, 0,
+                                     POS, COS, SIN, 4096, POS + 4096, 16, 1e-6, 0, 2, None), VALUE),
+    (lambda L: L.edge_qkv_rope_cache(QO, KO, KO + 65536, Q, WQ, WK, FP8, 4, 8, 2, 128, 64, 0,
+                                     POS, COS, SIN, 4096, POS + 4096, 16, 1e-6, 0, 1, None), DTYPE),
     (lambda L: rms(L, hidden=2 ** 25, rows=1), UNSUP),
 ])
 def test_invalid_calls_are_rejected(L, call, status):

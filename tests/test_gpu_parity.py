@@ -647,3 +647,83 @@ def test_quantize_fp8(dtype, n, mis):
     g.check()
     # exact: the input is exact in fp32, so both sides take the same fp32 decision
     assert np.array_equal(storage(g.t.cpu()), ref)
+
+
+# ---------------------------------------------------------------- fused QKV split + KV-cache write
+
+QKV_CASES = {
+    "text_bf16_d256_16x2": dict(dtype=torch.bfloat16, T=37, Hq=16, Hk=2, D=256, rot=64, layout=0,
+                                norm=True, offset=1, S=64),
+    "qwen_bf16_d128_32x8": dict(dtype=torch.bfloat16, T=64, Hq=32, Hk=8, D=128, rot=128, layout=0,
+                                norm=True, offset=0, S=100),
+    "f16_interleaved": dict(dtype=torch.float16, T=9, Hq=8, Hk=4, D=256, rot=256, layout=1,
+                            norm=True, offset=0, S=16),
+    "f32_d128": dict(dtype=torch.float32, T=5, Hq=8, Hk=2, D=128, rot=128, layout=0, norm=True,
+                     offset=1, S=8),
+    "no_norm_d256_8x1": dict(dtype=torch.bfloat16, T=10, Hq=8, Hk=1, D=256, rot=256, layout=0,
+                             norm=False, offset=0, S=12),
+    "decode_T1": dict(dtype=torch.bfloat16, T=1, Hq=24, Hk=4, D=256, rot=64, layout=0, norm=True,
+                      offset=1, S=4),
+    "prefill_T2000": dict(dtype=torch.bfloat16, T=2000, Hq=16, Hk=2, D=256, rot=64, layout=0,
+                          norm=True, offset=1, S=2048),
+}
+
+
+def run_qkv(c):
+    dtype, fmt = c["dtype"], TORCH_FMT[c["dtype"]]
+    T, Hq, Hk, D, S = c["T"], c["Hq"], c["Hk"], c["D"], c["S"]
+    qkv = synth.to_dtype(synth.normal(0, 71, T * (Hq + 2 * Hk) * D), dtype).view(T, -1)
+    wq = synth.to_dtype(synth.normal(0, 72, D, 0.0 if c["offset"] else 1.0, 0.05), dtype)
+    wk = synth.to_dtype(synth.normal(0, 73, D, 0.0 if c["offset"] else 1.0, 0.05), dtype)
+    P = 4096
+    cos, sin = synth.rope_cache(1e6, c["rot"], P)
+    pos = np.floor(synth.uniform(0, 74, T) * P).astype(np.int64)
+    pos[T // 3] = P            # out of cache: normalized, not rotated
+    slots = np.arange(T, dtype=np.int64) % S
+    if T > 2:
+        slots[1] = -1          # padding token: no cache write
+        slots[2] = S + 5       # out of range: no cache write
+    kc0 = synth.to_dtype(synth.normal(0, 75, S * Hk * D), dtype).view(S, Hk, D)
+    vc0 = synth.to_dtype(synth.normal(0, 76, S * Hk * D), dtype).view(S, Hk, D)
+    ref = oracle.qkv_rope_cache(storage(qkv), storage(wq), storage(wk), fmt, Hq, Hk, c["rot"],
+                                c["layout"], pos, storage(cos), storage(sin), slots, storage(kc0),
+                                storage(vc0), 1e-6, c["offset"], c["norm"], eta=ETA_NORM)
+    kc = Guarded((S, Hk, D), dtype)
+    vc = Guarded((S, Hk, D), dtype)
+    kc.t.copy_(kc0)
+    vc.t.copy_(vc0)
+    qo = Guarded((T, Hq, D), dtype)
+    edge_ops.qkv_rope_cache(dev(qkv), Hq, Hk, dev(wq), dev(wk), dev(torch.from_numpy(pos)),
+                            dev(cos), dev(sin), dev(torch.from_numpy(slots)), kc.t, vc.t,
+                            rotary_dim=c["rot"], layout=c["layout"], eps=1e-6,
+                            weight_offset=c["offset"], normalize=c["norm"], q_out=qo.t)
+    torch.cuda.synchronize()
+    for g in (kc, vc, qo):
+        g.check()
+    check_out("q", storage(qo.t.cpu()), ref.q_out, ref.q_pre, ref.q_mag, fmt, fmt, ETA_NORM,
+              lo=ref.q_lo, hi=ref.q_hi)
+    gk, gv = storage(kc.t.cpu()), storage(vc.t.cpu())
+    written = np.zeros(S, bool)
+    written[slots[(slots >= 0) & (slots < S)]] = True
+    # untouched rows keep their contents; value rows are exact copies
+    assert np.array_equal(gk[~written], storage(kc0)[~written])
+    assert np.array_equal(gv, ref.v_cache)
+    if written.any():
+        check_out("k_cache", gk[written], ref.k_cache[written], ref.k_pre[written],
+                  ref.k_mag[written], fmt, fmt, ETA_NORM, lo=ref.k_lo[written],
+                  hi=ref.k_hi[written])
+
+
+@pytest.mark.parametrize("name", list(QKV_CASES))
+def test_qkv_rope_cache(name):
+    run_qkv(QKV_CASES[name])
+
+
+def test_qkv_rope_cache_unsupported_shape_launches_nothing():
+    qkv = torch.zeros(2, 4 * 96, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 1, 96, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.zeros(2, dtype=torch.int64, device="cuda")
+    with pytest.raises(edge_ops.EdgeError, match="UNSUPPORTED"):
+        edge_ops.qkv_rope_cache(qkv, 2, 1, None, None, None, None, None, slots, kc, vc,
+                                rotary_dim=0)

@@ -524,3 +524,40 @@ def test_quantize_static_vs_torch(dtype):
     got = oracle.quantize_static(storage(x), FMT[dtype], float(inv))
     ref = (x.float() * torch.tensor(inv)).clamp(-448, 448).to(torch.float8_e4m3fn)
     assert np.array_equal(got, ref.view(torch.uint8).numpy())
+
+
+# ----------------------------------------------------------------- fused QKV split + KV-cache write
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_qkv_rope_cache_is_split_prologue_and_scatter(normalize):
+    T, Hq, Hk, D, rho, S = 6, 4, 2, 64, 32, 10
+    dtype, fmt = torch.bfloat16, oracle.BF16
+    rng = np.random.default_rng(61)
+    qkv = torch.from_numpy(rng.standard_normal((T, (Hq + 2 * Hk) * D))).to(dtype)
+    wq = torch.from_numpy(0.1 * rng.standard_normal(D)).to(dtype)
+    wk = torch.from_numpy(0.1 * rng.standard_normal(D)).to(dtype)
+    cos, sin = synth.rope_cache(1e4, rho, 16)
+    pos = np.array([0, 3, 15, 16, -1, 7])
+    slots = np.array([9, 0, -1, 4, 12, 5])
+    kc0 = storage(torch.from_numpy(rng.standard_normal((S, Hk, D))).to(dtype))
+    vc0 = storage(torch.from_numpy(rng.standard_normal((S, Hk, D))).to(dtype))
+    r = oracle.qkv_rope_cache(storage(qkv), storage(wq), storage(wk), fmt, Hq, Hk, rho,
+                              oracle.ROTATE_HALF, pos, storage(cos), storage(sin), slots, kc0, vc0,
+                              1e-6, 1, normalize)
+    x = storage(qkv).reshape(T, Hq + 2 * Hk, D)
+    q, k, v = x[:, :Hq], x[:, Hq:Hq + Hk], x[:, Hq + Hk:]
+    if normalize:
+        ref = oracle.qk_norm_rope(q, k, storage(wq), storage(wk), fmt, rho, oracle.ROTATE_HALF,
+                                  pos, storage(cos), storage(sin), 1e-6, 1)
+        rq, rk = ref.q_out, ref.k_out
+    else:
+        rq = oracle.rope(q, fmt, rho, oracle.ROTATE_HALF, pos, storage(cos), storage(sin))
+        rk = oracle.rope(k, fmt, rho, oracle.ROTATE_HALF, pos, storage(cos), storage(sin))
+    assert np.array_equal(r.q_out, rq)
+    for t in range(T):
+        if 0 <= slots[t] < S:
+            assert np.array_equal(r.k_cache[slots[t]], rk[t])
+            assert np.array_equal(r.v_cache[slots[t]], v[t])
+    untouched = [s for s in range(S) if s not in set(slots[(slots >= 0) & (slots < S)])]
+    assert np.array_equal(r.k_cache[untouched], kc0[untouched])
+    assert np.array_equal(r.v_cache[untouched], vc0[untouched])

@@ -39,6 +39,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -66,7 +67,7 @@ def parse():
     ap.add_argument("--impl", choices=["edge", "reference"], default="edge")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-t1", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=6.0)
     return ap.parse_args()
 
 
@@ -88,6 +89,24 @@ def bytes_qk(T, Hq, Hk, D, rot, s=2, out_s=2):
 
 def bytes_glu(T, d, s=2, out_s=2):
     return T * d * 2 * s + T * d * out_s
+
+
+def bytes_rope(T, Hq, Hk, D, rot, s=2, out_s=2):
+    return T * (Hq + Hk) * D * (s + out_s) + T * 8 + T * 2 * (rot // 2) * 4
+
+
+def bytes_layernorm(T, H, s=2, out_s=2, affine=True):
+    return T * H * (s + out_s) + (2 * H * s if affine else 0)
+
+
+def bytes_quant(n, s=2):
+    return n * (s + 1)
+
+
+def bytes_qkv_cache(T, Hq, Hk, D, rot, s=2):
+    # qkv read; q_out and the k/v cache rows written; weights, positions,
+    # slots and two cache rows of rot/2 fp32 per token
+    return 2 * T * (Hq + 2 * Hk) * D * s + 2 * D * s + 16 * T + T * 2 * (rot // 2) * 4
 
 
 def layer_bytes(T=T_DEC):
@@ -223,36 +242,84 @@ def oracle_layer(a):
     o.glu_act(a["gu"], o.BF16, o.SILU)
 
 
+def cpu_info():
+    """(logical cores, CPU model) of the host."""
+    model = platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return os.cpu_count() or 1, model
+
+
+def oracle_layers_for(a, seconds, threads):
+    """Run whole layers of the oracle for about `seconds` on `threads` host
+    threads (each runs its own layers; the C oracle releases the GIL), and
+    return (layers, elapsed seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    t0 = time.perf_counter()
+    deadline = t0 + seconds
+
+    def worker(_):
+        n = 0
+        while True:
+            oracle_layer(a)
+            n += 1
+            if time.perf_counter() >= deadline:
+                return n
+    if threads == 1:
+        n = worker(0)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            n = sum(ex.map(worker, range(threads)))
+    return n, time.perf_counter() - t0
+
+
 def cpu_baseline(seconds):
+    """The oracle as it stands on the host: single-threaded, and split over all
+    cores (one layer per thread at a time), `seconds` each."""
     a = oracle_layer_args(T_DEC)
     oracle_layer(a)
-    n, t0 = 0, time.perf_counter()
-    while True:
-        oracle_layer(a)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
+    cores, model = cpu_info()
+    n1, el1 = oracle_layers_for(a, seconds, 1)
+    n, el = oracle_layers_for(a, seconds, cores)
+    gbs1 = layer_bytes() * n1 / el1 / 1e9
     gbs = layer_bytes() * n / el / 1e9
-    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} of the workload's layers (T={T_DEC}, 4 ops each) in {el:.1f} s, "
-                      f"single-threaded C fp64 oracle on the host"}
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu": model, "ms_per_layer": round(el / n * 1e3, 3),
+            "single_thread": {"value": round(gbs1, 4), "unit": UNIT, "cores": 1,
+                              "ms_per_layer": round(el1 / n1 * 1e3, 3)},
+            "sample": f"{n} of the workload's layers (T={T_DEC}, 4 ops each) in {el:.1f} s on "
+                      f"{cores} threads (one layer each at a time), and {n1} layers in "
+                      f"{el1:.1f} s on one thread; the C fp64 oracle on the host"}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    T = 8  # bounded sample: 8 tokens of one layer per step
+    from concurrent.futures import ThreadPoolExecutor
+
+    T = 8  # bounded sample: 8 tokens of a layer per host thread per step
     a = oracle_layer_args(T)
-    for _ in range(args.warmup):
-        oracle_layer(a)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_layer(a)
-    el = time.perf_counter() - t0
-    gbs = layer_bytes(T) * args.steps / el / 1e9
-    sample = f"{T} tokens of one layer (4 ops) per step; single-threaded C fp64 oracle"
+    cores, model = cpu_info()
+    with ThreadPoolExecutor(cores) as ex:
+        def step():
+            list(ex.map(lambda _: oracle_layer(a), range(cores)))
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step()
+        el = time.perf_counter() - t0
+    gbs = cores * layer_bytes(T) * args.steps / el / 1e9
+    sample = (f"{T} tokens of one layer (4 ops) on each of {cores} host threads per step; "
+              f"the C fp64 oracle ({model})")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -260,8 +327,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "decode seams of a 36-layer decoder (reference arm: sample)",
                    "T": T, "hidden": HID, "gate": INTER, "heads": [HQ, HK], "head_dim": HD},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "cpu": model, "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -454,6 +521,22 @@ def sweep(torch, ops, synth, device, peak):
                                                 d["sin"], rotary_dim=64, weight_offset=1,
                                                 q_out=qo, k_out=ko)
             out[key][str(T)] = timed(make, bytes_qk(T, hq, hk, 256, 64))
+    # DFlash2 pair [128, 32, W, B]: 32 + 32 heads of 128, full rotary, direct
+    # weights, in place; W = 16 draft positions per sequence, B sequences
+    key = "qk_norm_rope_dflash2_bf16_32x32_d128_inplace_W16"
+    out[key] = {}
+    for B in (1, 4, 16, 64, 128):
+        T = 16 * B
+        i = synth.qk_inputs(0, bf, T, 32, 32, 128, 128, theta=1e6, cache_len=32768,
+                            positions="blocks:16", w_mean=1.0, w_std=0.02)
+        d = {k: v.to(device) for k, v in i.items()}
+
+        def make(d=d):
+            q, k = d["q"].clone(), d["k"].clone()
+            return lambda: ops.qk_norm_rope(q, k, d["wq"], d["wk"], d["positions"], d["cos"],
+                                            d["sin"], rotary_dim=128, weight_offset=0,
+                                            q_out=q, k_out=k)
+        out[key][f"B{B}"] = timed(make, bytes_qk(T, 32, 32, 128, 128))
     # residual-add RMSNorm, bf16 out and FP8 out
     for H in (2048, 1024, 2560):
         for fp8 in (False, True):
@@ -479,6 +562,58 @@ def sweep(torch, ops, synth, device, peak):
             o = torch.empty(T, 2048, dtype=torch.uint8, device=device)
             return lambda: ops.rmsnorm(x, None, eps=EPS, out=o, fp8=True, inv_scale=40.0)
         out[key][str(T)] = timed(make, bytes_rmsnorm(T, 2048, out_s=1, weight=False))
+    # standalone rotary, one-read LayerNorm, static FP8 quantize, fused QKV + KV write
+    key = "rope_bf16_24x4_d256_r64"
+    out[key] = {}
+    for T in (1, 64, 512, 2048):
+        i = synth.qk_inputs(0, bf, T, 24, 4, 256, 64, theta=1e7, cache_len=32768,
+                            positions="offset")
+        d = {k: v.to(device) for k, v in i.items() if v is not None}
+
+        def make(d=d):
+            q, k = d["q"].clone(), d["k"].clone()
+            qo, ko = torch.empty_like(q), torch.empty_like(k)
+            return lambda: ops.rope(q, k, d["positions"], d["cos"], d["sin"], rotary_dim=64,
+                                    q_out=qo, k_out=ko)
+        out[key][str(T)] = timed(make, bytes_rope(T, 24, 4, 256, 64))
+    key = "layernorm_bf16_h1152"
+    out[key] = {}
+    for T in (1, 64, 512, 4096):
+        i = synth.rows_inputs(0, bf, T, 1152)
+        x0, g = i["x"].to(device), i["w"].to(device)
+
+        def make(x0=x0, g=g):
+            x = x0.clone()
+            o = torch.empty_like(x)
+            return lambda: ops.layernorm(x, g, g, eps=1e-6, out=o)
+        out[key][str(T)] = timed(make, bytes_layernorm(T, 1152))
+    key = "quantize_fp8_bf16_rows_x2048"
+    out[key] = {}
+    for T in (1, 512, 4096):
+        x0 = synth.rows_inputs(0, bf, T, 2048, residual=False)["x"].to(device)
+
+        def make(x0=x0):
+            x = x0.clone()
+            o = torch.empty(x.shape, dtype=torch.uint8, device=device)
+            return lambda: ops.quantize_fp8(x, 40.0, out=o)
+        out[key][str(T)] = timed(make, bytes_quant(T * 2048))
+    key = "qkv_rope_cache_bf16_16x2_d256_r64"
+    out[key] = {}
+    for T in (1, 64, 512, 2048):
+        qkv0 = synth.to_dtype(synth.normal(0, 71, T * 20 * 256), bf).view(T, -1).to(device)
+        w = synth.to_dtype(synth.normal(0, 72, 256, 0.0, 0.05), bf).to(device)
+        cos, sin = synth.rope_cache(1e7, 64, 32768)
+        cos, sin = cos.to(device), sin.to(device)
+        pos = torch.arange(T, dtype=torch.int64, device=device)
+
+        def make(qkv0=qkv0, w=w, cos=cos, sin=sin, pos=pos, T=T):
+            qkv = qkv0.clone()
+            kc = torch.empty(T, 2, 256, dtype=bf, device=device)
+            vc = torch.empty_like(kc)
+            qo = torch.empty(T, 16, 256, dtype=bf, device=device)
+            return lambda: ops.qkv_rope_cache(qkv, 16, 2, w, w, pos, cos, sin, pos, kc, vc,
+                                              rotary_dim=64, weight_offset=1, q_out=qo)
+        out[key][str(T)] = timed(make, bytes_qkv_cache(T, 16, 2, 256, 64))
     # gates
     for name, d_, act, fp8 in (("glu_silu_bf16_d9728", INTER, ops.SILU, False),
                                ("glu_gelu_bf16_d2048_fp8", 2048, ops.GELU_TANH, True),

@@ -217,14 +217,18 @@ edge_status edge_quantize_fp8(void* out, const void* x, edge_dtype dt, int64_t n
  *        receives the key heads of token t after the same prologue, and the
  *        value heads unchanged.  A token whose slot is negative or
  *        >= num_slots writes no cache row, so the cache is never written out
- *        of bounds; the other rows are left untouched.
+ *        of bounds; the other rows are left untouched.  When two tokens name
+ *        the same slot, which token's row remains there is unspecified.
  * slots: [tokens] int64, device.  Caches and slots may be NULL when
  *        kv_heads == 0 or num_slots == 0.
+ * slots == NULL with num_slots == 0 writes no cache row at all (the query
+ * heads are still produced).
  * Output dtype is dt (no FP8 epilogue).  Outputs must not overlap each other
- * or any input.  This build has a vectorized path only: head_dim * size(dt) a
- * power-of-two multiple of 16 up to 512 bytes, 16-byte aligned tensors, and a
- * rotary width like edge_qk_norm_rope's vector path.  Other valid shapes
- * return EDGE_ERR_UNSUPPORTED without launching.
+ * or any input.  Element-aligned tensors of any head size up to 2048 are
+ * served: a vector path when head_dim * size(dt) is a power-of-two multiple
+ * of 16 up to 512 bytes, the tensors are 16-byte aligned and the rotary width
+ * suits 16-byte vectors, else a scalar path.  EDGE_ERR_UNSUPPORTED: head_dim
+ * above 2048, or tokens * (q_heads + 2 kv_heads) above 2^31 - 1.
  */
 edge_status edge_qkv_rope_cache(void* q_out, void* k_cache, void* v_cache, const void* qkv,
                                 const void* wq, const void* wk, edge_dtype dt, int64_t tokens,

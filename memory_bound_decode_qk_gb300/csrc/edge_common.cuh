@@ -165,66 +165,6 @@ __device__ __forceinline__ float inv_rms(float ss, float inv_n, float eps) {
     return rsqrtf(__fmaf_rn(ss, inv_n, eps));
 }
 
-// ---------------------------------------------------------------- bulk copies
-
-// Shared-memory address of a generic pointer into this CTA's shared memory.
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-// Make barrier initialization visible to the async (bulk-copy) proxy.
-__device__ __forceinline__ void mbar_init_fence() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// Order this thread's earlier generic-proxy shared accesses before later
-// bulk copies into the same shared memory.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-// One bulk copy global -> this CTA's shared memory (16-byte aligned ends,
-// size a multiple of 16), completing on barrier `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for phase `parity` of barrier `bar`.  Returns false after
-// kSpinLimit polls (each poll may itself suspend for a short while); the
-// caller then records the failure instead of waiting forever.
-constexpr uint32_t kSpinLimit = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-    }
-    return false;
-}
-
 // ---------------------------------------------------------------- PDL hooks
 
 // Programmatic dependent launch.  Both instructions are no-ops unless the
@@ -237,5 +177,37 @@ __device__ __forceinline__ void pdl_wait() {
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// ---------------------------------------------------------------- L2 prefetch
+
+// Ask L2 to fetch the bytes [base + lo, base + hi) from HBM (at most the
+// first kPrefetchMax of them).  Issued by one thread before pdl_wait(), the
+// fetch overlaps the HBM latency of a CTA's first loads with the tail of the
+// preceding grid.  A prefetch is a hint that returns no data: the loads that
+// read the bytes still come after the wait, and L2 stays coherent with every
+// SM's writes, so the preceding grid's writes to the range are still seen.
+// The start is rounded up and the end down to 16 bytes (the bulk prefetch
+// wants 16-byte-aligned addresses and sizes), so nothing outside the range is
+// touched.
+constexpr uint32_t kPrefetchPiece = 16u << 10;
+constexpr uint32_t kPrefetchMax = 64u << 10;
+__device__ __forceinline__ void prefetch_l2(const void* base, int64_t lo, int64_t hi) {
+    if (base == nullptr || hi <= lo) return;
+    const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+    uintptr_t s = (b + (uintptr_t)lo + 15u) & ~(uintptr_t)15u;
+    uintptr_t e = (b + (uintptr_t)hi) & ~(uintptr_t)15u;
+    if (e > s + kPrefetchMax) e = s + kPrefetchMax;
+    while (s < e) {
+        const uint32_t n = (uint32_t)(e - s < kPrefetchPiece ? e - s : kPrefetchPiece);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s), "r"(n) : "memory");
+        s += n;
+    }
+}
+
+// Prefetch into L2 the line holding *p (no alignment needed).
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+    if (p != nullptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 
 }  // namespace edge

@@ -11,6 +11,7 @@
 #include <cstdlib>
 #include <atomic>
 #include <initializer_list>
+#include <mutex>
 
 #include "../../include/edge_ops.h"
 #include "launch.h"
@@ -31,6 +32,32 @@ int sm_count() {
         n = 148;
     }
     if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int resident_ctas(const void* fn, int threads) {
+    struct Entry {
+        const void* fn;
+        int threads, dev, n;
+    };
+    static std::mutex mu;
+    static Entry table[128];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        if (table[i].fn == fn && table[i].threads == threads && table[i].dev == dev) {
+            return table[i].n;
+        }
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    if (n < 1) n = 1;
+    if (used < 128) table[used++] = Entry{fn, threads, dev, n};
     return n;
 }
 

@@ -130,6 +130,26 @@ __global__ void __launch_bounds__(256) glu_vec_kernel(GluP p) {
     const uint4* gu = reinterpret_cast<const uint4*>(p.gu);
     const uint32_t stride = gridDim.x * blockDim.x * U;
 
+    if (threadIdx.x == 0) {
+        // this CTA's first vectors into L2 while the preceding grid drains:
+        // flat vectors [i0, i1) lie in rows r0..r1, gate then up in each row
+        const uint32_t i0 = blockIdx.x * blockDim.x * U;
+        const uint32_t i1 = i0 + blockDim.x * U < p.total ? i0 + blockDim.x * U : p.total;
+        if (i0 < i1) {
+            const int64_t r0 = fast_div(i0, p.dv), r1 = fast_div(i1 - 1, p.dv);
+            const int64_t row = 32 * (int64_t)dv;  // bytes of one [g | u] row
+            if (r1 > r0 + 1) {
+                prefetch_l2(p.gu, r0 * row, (r1 + 1) * row);
+            } else {
+                for (int64_t r = r0; r <= r1; ++r) {
+                    const int64_t c0 = (int64_t)i0 > r * dv ? (int64_t)i0 - r * dv : 0;
+                    const int64_t c1 = (int64_t)i1 < (r + 1) * dv ? (int64_t)i1 - r * dv : dv;
+                    prefetch_l2(p.gu, r * row + 16 * c0, r * row + 16 * c1);
+                    prefetch_l2(p.gu, r * row + 16 * (dv + c0), r * row + 16 * (dv + c1));
+                }
+            }
+        }
+    }
     pdl_wait();
     pdl_launch_dependents();
 

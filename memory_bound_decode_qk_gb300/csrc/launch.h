@@ -92,6 +92,10 @@ cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
+// CTAs of kernel `fn` resident per SM at `threads` threads and no dynamic
+// shared memory (the occupancy calculator, cached per kernel and device).
+int resident_ctas(const void* fn, int threads);
+
 // Programmatic dependent launch for all ops (on unless EDGE_OPS_PDL=0 in the
 // environment, read once per process).  Every kernel executes
 // griddepcontrol.wait before its first global access, so it is always safe as

@@ -47,6 +47,31 @@ struct Unit {
     int64_t t;
 };
 
+// Prefetch into L2 what a CTA's first head units [u0, u1) read, before the
+// dependent-launch wait.  Token-major units (q heads then k heads of each
+// token) when `token_major`, else all q rows first and then all k rows.  CTA 0
+// also fetches the two norm weights.
+__device__ __forceinline__ void prefetch_heads(const QKP& p, uint32_t u0, uint32_t u1,
+                                               bool token_major) {
+    if (u1 > p.units) u1 = p.units;
+    if (u0 >= u1) return;
+    const int64_t hb = (int64_t)p.D * p.in_bytes;
+    if (token_major) {
+        const int64_t t0 = fast_div(u0, p.heads), t1 = fast_div(u1 - 1, p.heads) + 1;
+        prefetch_l2(p.q, t0 * p.q_heads * hb, t1 * p.q_heads * hb);
+        prefetch_l2(p.k, t0 * p.k_heads * hb, t1 * p.k_heads * hb);
+        if (p.rot > 0) prefetch_l2_line(p.pos + t0);
+    } else {
+        const uint32_t qr = p.qrows;
+        if (u0 < qr) prefetch_l2(p.q, (int64_t)u0 * hb, (int64_t)(u1 < qr ? u1 : qr) * hb);
+        if (u1 > qr) prefetch_l2(p.k, (int64_t)(u0 > qr ? u0 - qr : 0) * hb, (int64_t)(u1 - qr) * hb);
+    }
+    if (blockIdx.x == 0) {
+        prefetch_l2(p.wq, 0, hb);
+        prefetch_l2(p.wk, 0, hb);
+    }
+}
+
 __device__ __forceinline__ Unit locate(const QKP& p, uint32_t u) {
     uint32_t t = fast_div(u, p.heads);
     int h = (int)(u - t * p.heads.d);
@@ -230,10 +255,94 @@ __device__ __forceinline__ void weights_plus_delta(const QKP& p, const char* wpt
 // Threads-per-head path for many heads (qk_quad.cu).  *handled is false when
 // the geometry is outside its instantiations; the caller then takes the
 // lane-group path.
+// ---------------------------------------------------------------- generic head
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const char* base, int i) {
+    return to_f(reinterpret_cast<const T*>(base)[i]);
+}
+
+// One head of any size or alignment, by one warp, staged as fp32 in hm[D]
+// (shared memory).  With `norm` the head is normalized and weighted, and the
+// staged value is what the rotation consumes: rounded to T, or left in fp32
+// in the unrounded mode.  The first p.rot channels rotate when token t's
+// position is inside the cache.  Every output is rounded once to T (or takes
+// the FP8 epilogue).
+template <typename T, bool FP8>
+__device__ void generic_head(const QKP& p, const char* src, char* dst, const char* w, int64_t t,
+                             bool norm, float* hm, int lane, int layout) {
+    float ss = 0.0f;
+    for (int e = lane; e < p.D; e += 32) {
+        const float v = ld_elem<T>(src, e);
+        hm[e] = v;
+        ss = __fmaf_rn(v, v, ss);
+    }
+    if (norm) {
+        ss = group_sum<32>(ss);
+        const float r = inv_rms(ss, p.invD, p.eps);
+        const bool unrounded = (p.mode & kModeUnrounded) != 0;
+        for (int e = lane; e < p.D; e += 32) {
+            const float wd = w ? __fadd_rn(ld_elem<T>(w, e), p.delta) : 1.0f;
+            const float n = __fmul_rn(__fmul_rn(hm[e], r), wd);
+            hm[e] = unrounded ? n : round_to<T>(n);
+        }
+    }
+    __syncwarp();
+    int64_t pos = -1;
+    if (p.rot > 0) pos = p.pos[t];
+    const bool rot = pos >= 0 && pos < p.cache_len;
+    for (int e = lane; e < p.D; e += 32) {
+        float y = round_to<T>(hm[e]);
+        if (rot && e < p.rot) {
+            int j, partner;
+            bool first;
+            if (layout == kInterleaved) {
+                j = e >> 1;
+                partner = e ^ 1;
+                first = (e & 1) == 0;
+            } else {
+                first = e < p.half;
+                j = first ? e : e - p.half;
+                partner = first ? e + p.half : e - p.half;
+            }
+            const float c = p.cs[pos * p.half + j];
+            const float sn = p.sn[pos * p.half + j];
+            const float own = hm[e], other = hm[partner];
+            y = first ? __fmaf_rn(own, c, -__fmul_rn(other, sn))
+                      : __fmaf_rn(own, c, __fmul_rn(other, sn));
+        }
+        if constexpr (FP8) {
+            reinterpret_cast<uint8_t*>(dst)[e] = quantize1(y, p.inv);
+        } else {
+            reinterpret_cast<T*>(dst)[e] = from_f<T>(y);
+        }
+    }
+    __syncwarp();
+}
+
 template <typename T, bool FP8>
 cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg, bool* handled);
 
-// Whether the threads-per-head path is the better choice for this call.
-bool qk_quad_preferred(const QKArgs& a, int sms);
+// Whether the four-threads-per-head path suits a geometry once the
+// lane-group path's grid exceeds one wave of resident CTAs.
+bool quad_suits(int layout, int rotary_dim, int64_t head_bytes);
+
+// Arguments of the fused QKV kernels: the prologue's QKP (q = the fused qkv
+// rows, qo = q_out; k and ko unused) and the cache side.
+struct QKVP {
+    QKP p;
+    char* kc;              // k_cache
+    char* vc;              // v_cache
+    const int64_t* slots;  // nullable: no cache rows
+    int64_t num_slots;
+    int64_t row_bytes;     // bytes of one qkv row
+    FastDiv per_token;     // Hq + 2 Hk
+};
+
+// The four-threads-per-head path for the fused QKV op; *handled is false
+// when the geometry or alignment is outside the path (nothing launched).
+template <typename T>
+cudaError_t launch_qkv_quad(const QKVArgs& a, const QKVP& k, cudaLaunchConfig_t cfg,
+                            bool* handled);
 
 }  // namespace edge

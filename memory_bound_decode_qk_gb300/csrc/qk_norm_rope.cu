@@ -40,6 +40,10 @@ __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
 
+    if (threadIdx.x == 0) {
+        const uint32_t per_cta = (blockDim.x >> 5) * HPW;
+        prefetch_heads(p, blockIdx.x * per_cta, (blockIdx.x + 1) * per_cta, true);
+    }
     pdl_wait();
     pdl_launch_dependents();
 
@@ -65,11 +69,6 @@ __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
 
 // ---------------------------------------------------------------- generic path
 
-template <typename T>
-__device__ __forceinline__ float ld_elem(const char* base, int i) {
-    return to_f(reinterpret_cast<const T*>(base)[i]);
-}
-
 template <typename T, bool FP8>
 __global__ void __launch_bounds__(128) qk_generic_kernel(QKP p, int layout) {
     extern __shared__ float smem[];
@@ -83,61 +82,21 @@ __global__ void __launch_bounds__(128) qk_generic_kernel(QKP p, int layout) {
     pdl_launch_dependents();
 
     for (uint32_t u = warp; u < p.units; u += nwarps) {
-        Unit un = locate(p, u);
-        float ss = 0.0f;
-        for (int e = lane; e < p.D; e += 32) {
-            float v = ld_elem<T>(un.src, e);
-            hm[e] = v;
-            ss = __fmaf_rn(v, v, ss);
-        }
-        const bool norm = (p.mode & kModeNorm) != 0;
-        const bool unrounded = (p.mode & kModeUnrounded) != 0;
-        if (norm) {
-            ss = group_sum<32>(ss);
-            const float r = inv_rms(ss, p.invD, p.eps);
-            // the staged value is what the rotation consumes: the normalized
-            // value, rounded to the dtype unless in the unrounded mode
-            for (int e = lane; e < p.D; e += 32) {
-                float w = un.w ? __fadd_rn(ld_elem<T>(un.w, e), p.delta) : 1.0f;
-                const float n = __fmul_rn(__fmul_rn(hm[e], r), w);
-                hm[e] = unrounded ? n : round_to<T>(n);
-            }
-        }
-        __syncwarp();
-        int64_t pos = -1;
-        if (p.rot > 0) pos = p.pos[un.t];
-        const bool rot = pos >= 0 && pos < p.cache_len;
-        for (int e = lane; e < p.D; e += 32) {
-            float y = round_to<T>(hm[e]);
-            if (rot && e < p.rot) {
-                int j, partner;
-                bool first;
-                if (layout == kInterleaved) {
-                    j = e >> 1;
-                    partner = e ^ 1;
-                    first = (e & 1) == 0;
-                } else {
-                    first = e < p.half;
-                    j = first ? e : e - p.half;
-                    partner = first ? e + p.half : e - p.half;
-                }
-                const float c = p.cs[pos * p.half + j];
-                const float sn = p.sn[pos * p.half + j];
-                const float own = hm[e], other = hm[partner];
-                y = first ? __fmaf_rn(own, c, -__fmul_rn(other, sn))
-                          : __fmaf_rn(own, c, __fmul_rn(other, sn));
-            }
-            if constexpr (FP8) {
-                reinterpret_cast<uint8_t*>(un.dst)[e] = quantize1(y, p.inv);
-            } else {
-                reinterpret_cast<T*>(un.dst)[e] = from_f<T>(y);
-            }
-        }
-        __syncwarp();
+        const Unit un = locate(p, u);
+        generic_head<T, FP8>(p, un.src, un.dst, un.w, un.t, (p.mode & kModeNorm) != 0, hm, lane,
+                             layout);
     }
 }
 
 // ---------------------------------------------------------------- launch
+
+using QKFn = void (*)(QKP);
+
+template <typename T, bool FP8, int LPH>
+QKFn vec_fn(int layout) {
+    return layout == kInterleaved ? qk_vec_kernel<T, FP8, LPH, kInterleaved>
+                                  : qk_vec_kernel<T, FP8, LPH, kRotateHalf>;
+}
 
 template <typename T, bool FP8>
 cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
@@ -170,12 +129,14 @@ cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
     if (vec) {
         const int lph = nvec;
         const int hpw = 32 / lph;
-        int path = qk_path_override();
-        if (path == 0) path = qk_quad_preferred(a, sms) ? 3 : 1;
-        if (path == 3) {
-            bool handled = false;
-            cudaError_t e = launch_qk_quad<T, FP8>(a, p, cfg, &handled);
-            if (handled || e != cudaSuccess) return e;
+        QKFn vfn = nullptr;
+        switch (lph) {
+            case 1: vfn = vec_fn<T, FP8, 1>(a.layout); break;
+            case 2: vfn = vec_fn<T, FP8, 2>(a.layout); break;
+            case 4: vfn = vec_fn<T, FP8, 4>(a.layout); break;
+            case 8: vfn = vec_fn<T, FP8, 8>(a.layout); break;
+            case 16: vfn = vec_fn<T, FP8, 16>(a.layout); break;
+            default: vfn = vec_fn<T, FP8, 32>(a.layout); break;
         }
         // decode-width path: one head per lane group, a one-shot grid (on
         // GB300 many short CTAs that each issue one round of loads keep more
@@ -184,27 +145,28 @@ cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
         const int threads = 256;
         const int64_t per_block = (int64_t)(threads / 32) * hpw;
         int64_t blocks = ((int64_t)p.units + per_block - 1) / per_block;
+        int path = qk_path_override();
+        if (path == 0) {
+            // Measured on GB300 for every geometry: the one-shot grid wins
+            // while it fits in one wave of resident CTAs; past that, four
+            // threads per head (about 4x fewer instructions per head) win.
+            const int64_t wave = (int64_t)resident_ctas((const void*)vfn, threads) * sms;
+            path = blocks > wave &&
+                           quad_suits(a.layout, a.rotary_dim, (int64_t)D * (int64_t)sizeof(T))
+                       ? 3
+                       : 1;
+        }
+        if (path == 3) {
+            bool handled = false;
+            cudaError_t e = launch_qk_quad<T, FP8>(a, p, cfg, &handled);
+            if (handled || e != cudaSuccess) return e;
+        }
         const int64_t cap = (int64_t)sms * (2048 / threads) * 64;
         if (blocks > cap) blocks = cap;
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(threads);
         cfg.dynamicSmemBytes = 0;
-#define EDGE_QK_CASE(L)                                                                 \
-    case L:                                                                              \
-        return a.layout == kInterleaved                                                 \
-                   ? cudaLaunchKernelEx(&cfg, qk_vec_kernel<T, FP8, L, kInterleaved>, p) \
-                   : cudaLaunchKernelEx(&cfg, qk_vec_kernel<T, FP8, L, kRotateHalf>, p);
-        switch (lph) {
-            EDGE_QK_CASE(1)
-            EDGE_QK_CASE(2)
-            EDGE_QK_CASE(4)
-            EDGE_QK_CASE(8)
-            EDGE_QK_CASE(16)
-            EDGE_QK_CASE(32)
-            default:
-                break;
-        }
-#undef EDGE_QK_CASE
+        return cudaLaunchKernelEx(&cfg, vfn, p);
     }
     const int threads = 128;
     const int64_t warps_per_block = threads / 32;

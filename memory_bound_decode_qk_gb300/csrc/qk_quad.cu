@@ -29,6 +29,11 @@
 // known at compile time.  About 50 warp-instructions per head remain.  All C
 // loads of a thread are issued before any arithmetic, so a warp (8 heads) has
 // 4 KB in flight.
+//
+// The same body serves the fused QKV op (qkv_cache.cu): a mapper gives each
+// head unit its source, destination and kind.  Value heads take the body with
+// a unit weight and no norm or rotation, so a warp never diverges on them and
+// their bits are copied exactly.
 #include "qk_common.cuh"
 
 namespace edge {
@@ -36,50 +41,130 @@ namespace {
 
 constexpr int K = 4;  // threads per head
 
+// CTAs per SM that the register budget is sized for (65536 registers per SM,
+// 256 threads per CTA).  Fewer elements per thread leave fewer live values,
+// so more CTAs fit: 5 (51 registers) for 128-byte heads and 4 (64) for
+// 256-byte heads, both without spills; 3 (85) for 512-byte heads; 2 (128)
+// with the FP8 epilogue, and for 16-bit 512-byte heads (64 elements per
+// thread) that are interleaved or have more than two rotate-half chunks per
+// thread.  Measured on GB300: those 16-bit heads ran faster at 2 CTAs than at
+// 3 with spills, while fp32 512-byte heads (32 elements per thread) ran
+// faster at 3 CTAs, spilling about a hundred bytes, than at 2.
+template <typename T, bool FP8, int C, int LAYOUT, int RQ>
+constexpr int quad_min_blocks() {
+    return FP8 ? 2
+               : C <= 2 ? 5
+               : C <= 4 ? 4
+               : (sizeof(T) == 2 && (LAYOUT == kInterleaved || 2 * RQ > 2)) ? 2 : 3;
+}
+
+constexpr int kKindQ = 0, kKindK = 1, kKindV = 2;
+
+// One head unit: where its chunks come from and go to.
+struct QuadUnit {
+    const char* src;
+    char* dst;     // nullptr: nothing to store (a cache head without a slot)
+    uint32_t t;    // token
+    int kind;      // kKindQ, kKindK or kKindV
+};
+
+// The two-tensor prologue: all q rows, then all k rows.  Every unit is a
+// query or key head with a destination.
+struct QKMap {
+    static constexpr bool kHasV = false;
+    __device__ __forceinline__ QuadUnit unit(const QKP& p, uint32_t u, uint32_t hb) const {
+        const bool isq = u < p.qrows;
+        const uint32_t row = isq ? u : u - p.qrows;
+        QuadUnit r;
+        r.t = fast_div(row, isq ? p.qdiv : p.kdiv);
+        r.src = (isq ? p.q : p.k) + (size_t)row * hb;
+        r.dst = (isq ? p.qo : p.ko) + (size_t)row * (size_t)p.D * p.out_bytes;
+        r.kind = isq ? kKindQ : kKindK;
+        return r;
+    }
+    __device__ __forceinline__ void prefetch(const QKP& p, uint32_t u0, uint32_t u1) const {
+        prefetch_heads(p, u0, u1, false);
+    }
+};
+
+// Fused QKV rows [Hq q heads | Hk k heads | Hk v heads] per token, token-major;
+// k and v heads go to row slots[t] of their cache (nowhere when out of range).
+struct QKVMap {
+    static constexpr bool kHasV = true;  // value heads, and units with no destination
+    const QKVP* a;
+    __device__ __forceinline__ QuadUnit unit(const QKP& p, uint32_t u, uint32_t hb) const {
+        const uint32_t t = fast_div(u, a->per_token);
+        const int h = (int)(u - t * a->per_token.d);
+        QuadUnit r;
+        r.t = t;
+        r.src = p.q + (int64_t)t * a->row_bytes + (int64_t)h * hb;
+        if (h < p.q_heads) {
+            r.kind = kKindQ;
+            r.dst = p.qo + ((int64_t)t * p.q_heads + h) * hb;
+        } else {
+            const bool isv = h >= p.q_heads + p.k_heads;
+            const int j = isv ? h - p.q_heads - p.k_heads : h - p.q_heads;
+            r.kind = isv ? kKindV : kKindK;
+            const int64_t slot = a->slots != nullptr ? __ldg(a->slots + t) : -1;
+            r.dst = (slot >= 0 && slot < a->num_slots)
+                        ? (isv ? a->vc : a->kc) + (slot * p.k_heads + j) * hb
+                        : nullptr;
+        }
+        return r;
+    }
+    __device__ __forceinline__ void prefetch(const QKP& p, uint32_t u0, uint32_t u1) const {
+        if (u1 > p.units) u1 = p.units;
+        if (u0 >= u1) return;
+        const int64_t t0 = fast_div(u0, a->per_token), t1 = fast_div(u1 - 1, a->per_token) + 1;
+        prefetch_l2(p.q, t0 * a->row_bytes, t1 * a->row_bytes);
+    }
+};
+
 // RQ: rotate-half: chunks per thread that are first members (HVQ); interleaved:
 // chunks per thread that rotate.  0: no channel rotates.
-template <typename T, bool FP8, int C, int LAYOUT, int RQ>
-__global__ void __launch_bounds__(256, FP8 ? 2 : 3) qk_quad_kernel(QKP p) {
+template <typename T, bool FP8, int C, int LAYOUT, int RQ, class Map>
+__device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
     constexpr int N = vec_elems<T>();
     constexpr int D = C * K * N;
     static_assert(LAYOUT == kInterleaved ? RQ <= C : 2 * RQ <= C, "rotated chunks exceed the head");
-    __shared__ __align__(16) float wsm[2][D];
+    // w + delta in fp32 (1 when no weight) for q heads, k heads, and 1 for v
+    __shared__ __align__(16) float wsm[3][D];
 
+    const int heads_per_cta = blockDim.x / K;
+    if (threadIdx.x == 0) {
+        map.prefetch(p, blockIdx.x * heads_per_cta, (blockIdx.x + 1) * heads_per_cta);
+    }
     pdl_wait();
     pdl_launch_dependents();
 
-    // w + delta in fp32 (1 when no weight), for q heads and k heads
     for (int e = threadIdx.x; e < D; e += blockDim.x) {
         const float dq = p.wq ? __fadd_rn(to_f(reinterpret_cast<const T*>(p.wq)[e]), p.delta) : 1.0f;
         const float dk = p.wk ? __fadd_rn(to_f(reinterpret_cast<const T*>(p.wk)[e]), p.delta) : 1.0f;
-        wsm[0][e] = dq;
-        wsm[1][e] = dk;
+        wsm[kKindQ][e] = dq;
+        wsm[kKindK][e] = dk;
+        wsm[kKindV][e] = 1.0f;
     }
     __syncthreads();
 
     const int kt = threadIdx.x & (K - 1);
     const int hs = threadIdx.x / K;           // head slot in the CTA
-    const int heads_per_cta = blockDim.x / K;
     const uint32_t hb = (uint32_t)D * sizeof(T);
 
     for (uint32_t base = blockIdx.x * heads_per_cta; base < p.units;
          base += gridDim.x * heads_per_cta) {
         const uint32_t u = base + hs;
         const bool active = u < p.units;
-        const bool isq = u < p.qrows;
-        const uint32_t row = isq ? u : u - p.qrows;
-        const uint32_t t = active ? fast_div(row, isq ? p.qdiv : p.kdiv) : 0;
-        const char* src = (isq ? p.q : p.k) + (size_t)row * hb;
-        char* dst = (isq ? p.qo : p.ko) + (size_t)row * D * p.out_bytes;
+        const QuadUnit un = map.unit(p, active ? u : base, hb);
 
         uint4 raw[C];
 #pragma unroll
         for (int i = 0; i < C; ++i) {
-            raw[i] = active ? __ldcs(reinterpret_cast<const uint4*>(src) + kt + K * i)
+            raw[i] = active ? __ldcs(reinterpret_cast<const uint4*>(un.src) + kt + K * i)
                             : make_uint4(0u, 0u, 0u, 0u);
         }
+        const bool isv = Map::kHasV && un.kind == kKindV;
         int64_t pos = -1;
-        if (RQ > 0 && active) pos = __ldg(p.pos + t);
+        if (RQ > 0 && active && !isv) pos = __ldg(p.pos + un.t);
 
         float ss = 0.0f;
 #pragma unroll
@@ -91,12 +176,16 @@ __global__ void __launch_bounds__(256, FP8 ? 2 : 3) qk_quad_kernel(QKP p) {
         }
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        // without normalization (standalone rotary) r = 1 and w = 1: m = x
-        const float r = (p.mode & kModeNorm) ? inv_rms(ss, p.invD, p.eps) : 1.0f;
+        // without normalization (standalone rotary, the unnormalized QKV
+        // form, value heads) r = 1 and w = 1: m = x exactly
+        const bool norm = (p.mode & kModeNorm) && !isv;
+        const float r = norm ? inv_rms(ss, p.invD, p.eps) : 1.0f;
 
         // normalized value rounded to the dtype, packed (exactly) over the
-        // loaded vectors, which are no longer needed
-        const float* w = wsm[isq ? 0 : 1];
+        // loaded vectors, which are no longer needed.  (The prologue's
+        // unnormalized form, standalone rotary, passes no weights, so its
+        // q/k rows hold 1.)
+        const float* w = wsm[Map::kHasV ? (norm ? un.kind : kKindV) : un.kind];
         uint4 (&mp)[C] = raw;
 #pragma unroll
         for (int i = 0; i < C; ++i) {
@@ -115,8 +204,8 @@ __global__ void __launch_bounds__(256, FP8 ? 2 : 3) qk_quad_kernel(QKP p) {
         }
 
         const bool rot = RQ > 0 && pos >= 0 && pos < p.cache_len;
-        if (!active) continue;
-        char* out = dst;
+        if (!active || (Map::kHasV && un.dst == nullptr)) continue;
+        char* out = un.dst;
         auto emit = [&](int i, const float (&y)[N]) {
             if constexpr (FP8) {
                 auto q8 = quantize_vec<N>(y, p.inv);
@@ -200,29 +289,89 @@ __global__ void __launch_bounds__(256, FP8 ? 2 : 3) qk_quad_kernel(QKP p) {
     }
 }
 
-using QuadFn = void (*)(QKP);
+template <typename T, bool FP8, int C, int LAYOUT, int RQ>
+__global__ void __launch_bounds__(256, (quad_min_blocks<T, FP8, C, LAYOUT, RQ>()))
+    qk_quad_kernel(QKP p) {
+    quad_body<T, FP8, C, LAYOUT, RQ>(p, QKMap{});
+}
+
+template <typename T, int C, int LAYOUT, int RQ>
+__global__ void __launch_bounds__(256, (quad_min_blocks<T, false, C, LAYOUT, RQ>()))
+    qkv_quad_kernel(QKVP a) {
+    quad_body<T, false, C, LAYOUT, RQ>(a.p, QKVMap{&a});
+}
+
+// Kernel selectors for pick_rq: the prologue (FP8 or not) and the fused QKV op.
+template <typename T, bool FP8, int C, int LAYOUT, int RQ>
+struct QKSel {
+    static constexpr void (*fn)(QKP) = qk_quad_kernel<T, FP8, C, LAYOUT, RQ>;
+};
+template <typename T, bool FP8, int C, int LAYOUT, int RQ>
+struct QKVSel {
+    static constexpr void (*fn)(QKVP) = qkv_quad_kernel<T, C, LAYOUT, RQ>;
+};
 
 // The instantiated (C, layout, RQ) combinations: head sizes of 2, 4 or 8
 // chunks per thread (D*s = 128, 256 or 512 bytes), every rotary width that
 // keeps pairs thread-local.
-template <typename T, bool FP8, int C>
-QuadFn pick_rq(int layout, int rq) {
-    if (rq == 0) return qk_quad_kernel<T, FP8, C, kRotateHalf, 0>;
+template <template <typename, bool, int, int, int> class Sel, typename T, bool FP8, int C>
+auto pick_rq(int layout, int rq) -> decltype(Sel<T, FP8, C, kRotateHalf, 0>::fn) {
+    if (rq == 0) return Sel<T, FP8, C, kRotateHalf, 0>::fn;
     if (layout == kInterleaved) {
         switch (rq) {
-            case 1: return qk_quad_kernel<T, FP8, C, kInterleaved, 1>;
-            case 2: return C >= 2 ? qk_quad_kernel<T, FP8, C, kInterleaved, (C >= 2 ? 2 : 1)> : nullptr;
-            case 4: return C >= 4 ? qk_quad_kernel<T, FP8, C, kInterleaved, (C >= 4 ? 4 : 1)> : nullptr;
-            case 8: return C >= 8 ? qk_quad_kernel<T, FP8, C, kInterleaved, (C >= 8 ? 8 : 1)> : nullptr;
+            case 1: return Sel<T, FP8, C, kInterleaved, 1>::fn;
+            case 2: return C >= 2 ? Sel<T, FP8, C, kInterleaved, (C >= 2 ? 2 : 1)>::fn : nullptr;
+            case 4: return C >= 4 ? Sel<T, FP8, C, kInterleaved, (C >= 4 ? 4 : 1)>::fn : nullptr;
+            case 8: return C >= 8 ? Sel<T, FP8, C, kInterleaved, (C >= 8 ? 8 : 1)>::fn : nullptr;
             default: return nullptr;
         }
     }
     switch (rq) {
-        case 1: return qk_quad_kernel<T, FP8, C, kRotateHalf, 1>;
-        case 2: return C >= 4 ? qk_quad_kernel<T, FP8, C, kRotateHalf, (C >= 4 ? 2 : 1)> : nullptr;
-        case 4: return C >= 8 ? qk_quad_kernel<T, FP8, C, kRotateHalf, (C >= 8 ? 4 : 1)> : nullptr;
+        case 1: return Sel<T, FP8, C, kRotateHalf, 1>::fn;
+        case 2: return C >= 4 ? Sel<T, FP8, C, kRotateHalf, (C >= 4 ? 2 : 1)>::fn : nullptr;
+        case 4: return C >= 8 ? Sel<T, FP8, C, kRotateHalf, (C >= 8 ? 4 : 1)>::fn : nullptr;
         default: return nullptr;
     }
+}
+
+// Chunks per thread C and rotated chunks RQ of a geometry the path takes, or
+// false: head bytes 128, 256 or 512; 16-byte aligned heads; a rotary width
+// whose pairs stay in one thread; cache rows aligned for their vector loads.
+template <typename T>
+bool quad_shape(int head_dim, int rot, int layout, const void* const* bufs, int nbufs,
+                const void* cs, const void* sn, int* C, int* rq) {
+    constexpr int N = vec_elems<T>();
+    const int64_t hb = (int64_t)head_dim * (int64_t)sizeof(T);
+    if (hb % (16 * K) != 0) return false;
+    *C = (int)(hb / (16 * K));
+    if (*C != 2 && *C != 4 && *C != 8) return false;
+    for (int i = 0; i < nbufs; ++i) {
+        if (bufs[i] != nullptr && reinterpret_cast<uintptr_t>(bufs[i]) % 16 != 0) return false;
+    }
+    *rq = 0;
+    if (rot > 0) {
+        const int unit = (layout == kInterleaved ? 1 : 2) * K * N;
+        if (rot % unit != 0) return false;
+        const uintptr_t ca = layout == kInterleaved ? 8 * (N / 4) : 16;
+        if (reinterpret_cast<uintptr_t>(cs) % ca != 0 || reinterpret_cast<uintptr_t>(sn) % ca != 0) {
+            return false;
+        }
+        *rq = rot / unit;
+    }
+    return true;
+}
+
+template <typename P, typename Fn>
+cudaError_t launch_quad(Fn fn, const P& arg, uint32_t units, cudaLaunchConfig_t cfg) {
+    const int threads = 256;
+    const int64_t per_block = threads / K;
+    int64_t blocks = ((int64_t)units + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)sm_count() * 64;
+    if (blocks > cap) blocks = cap;
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, fn, arg);
 }
 
 }  // namespace
@@ -232,53 +381,52 @@ cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg
     constexpr int N = vec_elems<T>();
     *handled = false;
     if (a.mode & kModeUnrounded) return cudaSuccess;  // served by the lane-group path
-    const int64_t hb = (int64_t)a.head_dim * (int64_t)sizeof(T);
-    if (hb % (16 * K) != 0) return cudaSuccess;
-    const int C = (int)(hb / (16 * K));
-    if (C != 2 && C != 4 && C != 8) return cudaSuccess;
-    auto aligned = [](const void* ptr, uintptr_t n) {
-        return ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) % n) == 0;
-    };
-    if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.q_out, FP8 ? N : 16) ||
-        !aligned(a.k_out, FP8 ? N : 16)) {
+    // FP8 outputs are N bytes per chunk: alignment N
+    if ((a.q_out && reinterpret_cast<uintptr_t>(a.q_out) % (FP8 ? N : 16) != 0) ||
+        (a.k_out && reinterpret_cast<uintptr_t>(a.k_out) % (FP8 ? N : 16) != 0)) {
         return cudaSuccess;
     }
-    int rq = 0;
-    if (p.rot > 0) {
-        const int unit = (a.layout == kInterleaved ? 1 : 2) * K * N;
-        if (p.rot % unit != 0) return cudaSuccess;
-        if (!aligned(a.cos, a.layout == kInterleaved ? 8 * (N / 4) : 16) ||
-            !aligned(a.sin, a.layout == kInterleaved ? 8 * (N / 4) : 16)) {
-            return cudaSuccess;
-        }
-        rq = p.rot / unit;
+    const void* bufs[2] = {a.q, a.k};
+    int C = 0, rq = 0;
+    if (!quad_shape<T>(a.head_dim, p.rot, a.layout, bufs, 2, a.cos, a.sin, &C, &rq)) {
+        return cudaSuccess;
     }
-    QuadFn fn = nullptr;
+    void (*fn)(QKP) = nullptr;
     switch (C) {
-        case 2: fn = pick_rq<T, FP8, 2>(a.layout, rq); break;
-        case 4: fn = pick_rq<T, FP8, 4>(a.layout, rq); break;
-        default: fn = pick_rq<T, FP8, 8>(a.layout, rq); break;
+        case 2: fn = pick_rq<QKSel, T, FP8, 2>(a.layout, rq); break;
+        case 4: fn = pick_rq<QKSel, T, FP8, 4>(a.layout, rq); break;
+        default: fn = pick_rq<QKSel, T, FP8, 8>(a.layout, rq); break;
     }
     if (fn == nullptr) return cudaSuccess;
     *handled = true;
-    const int threads = 256;
-    const int64_t per_block = threads / K;
-    int64_t blocks = ((int64_t)p.units + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)sm_count() * 64;
-    if (blocks > cap) blocks = cap;
-    cfg.gridDim = dim3((unsigned)blocks);
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, fn, p);
+    return launch_quad(fn, p, p.units, cfg);
 }
 
-bool qk_quad_preferred(const QKArgs& a, int sms) {
-    // Measured crossover on GB300 (bf16, head_dim 256): the lane-group path
-    // wins below about 40 heads per SM (decode widths, where its one-shot grid
-    // puts every head in flight at once), this path above (it issues ~4x fewer
-    // instructions per head).
-    const int64_t units = a.tokens * (int64_t)(a.q_heads + a.k_heads);
-    return units >= (int64_t)sms * 40;
+template <typename T>
+cudaError_t launch_qkv_quad(const QKVArgs& a, const QKVP& k, cudaLaunchConfig_t cfg,
+                            bool* handled) {
+    *handled = false;
+    const void* bufs[4] = {a.qkv, a.q_out, a.k_cache, a.v_cache};
+    int C = 0, rq = 0;
+    if (!quad_shape<T>(a.head_dim, k.p.rot, a.layout, bufs, 4, a.cos, a.sin, &C, &rq)) {
+        return cudaSuccess;
+    }
+    void (*fn)(QKVP) = nullptr;
+    switch (C) {
+        case 2: fn = pick_rq<QKVSel, T, false, 2>(a.layout, rq); break;
+        case 4: fn = pick_rq<QKVSel, T, false, 4>(a.layout, rq); break;
+        default: fn = pick_rq<QKVSel, T, false, 8>(a.layout, rq); break;
+    }
+    if (fn == nullptr) return cudaSuccess;
+    *handled = true;
+    return launch_quad(fn, k, k.p.units, cfg);
+}
+
+bool quad_suits(int layout, int rotary_dim, int64_t head_bytes) {
+    // 512-byte heads in the interleaved layout need the two-CTA register
+    // budget, and measured no faster than the lane-group path at any width
+    // on GB300
+    return !(layout == kInterleaved && rotary_dim > 0 && head_bytes == 512);
 }
 
 template cudaError_t launch_qk_quad<float, false>(const QKArgs&, const QKP&, cudaLaunchConfig_t, bool*);
@@ -287,5 +435,8 @@ template cudaError_t launch_qk_quad<__half, false>(const QKArgs&, const QKP&, cu
 template cudaError_t launch_qk_quad<__half, true>(const QKArgs&, const QKP&, cudaLaunchConfig_t, bool*);
 template cudaError_t launch_qk_quad<__nv_bfloat16, false>(const QKArgs&, const QKP&, cudaLaunchConfig_t, bool*);
 template cudaError_t launch_qk_quad<__nv_bfloat16, true>(const QKArgs&, const QKP&, cudaLaunchConfig_t, bool*);
+template cudaError_t launch_qkv_quad<float>(const QKVArgs&, const QKVP&, cudaLaunchConfig_t, bool*);
+template cudaError_t launch_qkv_quad<__half>(const QKVArgs&, const QKVP&, cudaLaunchConfig_t, bool*);
+template cudaError_t launch_qkv_quad<__nv_bfloat16>(const QKVArgs&, const QKVP&, cudaLaunchConfig_t, bool*);
 
 }  // namespace edge

@@ -23,16 +23,6 @@
 namespace edge {
 namespace {
 
-struct QKVP {
-    QKP p;                 // q_heads, k_heads, D, rot, cache, eps, weights, q output
-    char* kc;              // k_cache
-    char* vc;              // v_cache
-    const int64_t* slots;
-    int64_t num_slots;
-    int64_t row_bytes;     // bytes of one qkv row
-    FastDiv per_token;     // Hq + 2 Hk
-};
-
 template <typename T, int LPH, int LAYOUT>
 __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
     constexpr int N = vec_elems<T>();
@@ -45,6 +35,17 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     const int hb = p.D * (int)sizeof(T);
 
+    if (threadIdx.x == 0) {
+        // the qkv rows of this CTA's first units into L2 while the preceding
+        // grid drains
+        const uint32_t per_cta = (blockDim.x >> 5) * HPW;
+        const uint32_t u0 = blockIdx.x * per_cta;
+        const uint32_t u1 = u0 + per_cta < p.units ? u0 + per_cta : p.units;
+        if (u0 < u1) {
+            const int64_t t0 = fast_div(u0, a.per_token), t1 = fast_div(u1 - 1, a.per_token) + 1;
+            prefetch_l2(p.q, t0 * a.row_bytes, t1 * a.row_bytes);
+        }
+    }
     pdl_wait();
     pdl_launch_dependents();
 
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
         if (active) {
             raw = __ldcs(reinterpret_cast<const uint4*>(src) + sub);
             if (p.rot > 0 && !isv) pos = __ldg(p.pos + t);
-            if (!isq) slot = __ldg(a.slots + t);
+            if (!isq && a.slots != nullptr) slot = __ldg(a.slots + t);
         }
         char* dst = nullptr;
         if (isq) {
@@ -80,6 +81,54 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
         qk_core<T, false, LPH, LAYOUT>(p, dst, active && dst != nullptr, lane, sub, raw, w, role,
                                        cr, isv);
     }
+}
+
+// Any head size or alignment: one warp per head, staged in shared memory.
+template <typename T>
+__global__ void __launch_bounds__(128) qkv_generic_kernel(QKVP a, int layout) {
+    extern __shared__ float qkv_smem[];
+    const QKP& p = a.p;
+    const int lane = threadIdx.x & 31;
+    float* hm = qkv_smem + (threadIdx.x >> 5) * p.D;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int64_t hb = (int64_t)p.D * (int64_t)sizeof(T);
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (uint32_t u = warp; u < p.units; u += nwarps) {
+        const uint32_t t = fast_div(u, a.per_token);
+        const int h = (int)(u - t * a.per_token.d);
+        const char* src = p.q + (int64_t)t * a.row_bytes + h * hb;
+        const bool isq = h < p.q_heads;
+        const bool isv = h >= p.q_heads + p.k_heads;
+        const int j = isq ? h : (isv ? h - p.q_heads - p.k_heads : h - p.q_heads);
+        char* dst;
+        if (isq) {
+            dst = p.qo + ((int64_t)t * p.q_heads + j) * hb;
+        } else {
+            // no cache (slots NULL) or a slot outside it: no cache row; the
+            // same for the whole warp
+            const int64_t slot = a.slots != nullptr ? a.slots[t] : -1;
+            if (slot < 0 || slot >= a.num_slots) continue;
+            dst = (isv ? a.vc : a.kc) + (slot * p.k_heads + j) * hb;
+        }
+        if (isv) {
+            for (int e = lane; e < p.D; e += 32) {
+                reinterpret_cast<T*>(dst)[e] = reinterpret_cast<const T*>(src)[e];
+            }
+        } else {
+            generic_head<T, false>(p, src, dst, isq ? p.wq : p.wk, t, (p.mode & kModeNorm) != 0,
+                                   hm, lane, layout);
+        }
+    }
+}
+
+template <typename T, int LPH>
+void (*qkv_vec_fn(int layout))(QKVP) {
+    return layout == kInterleaved ? qkv_vec_kernel<T, LPH, kInterleaved>
+                                  : qkv_vec_kernel<T, LPH, kRotateHalf>;
 }
 
 template <typename T>
@@ -101,15 +150,7 @@ cudaError_t launch_typed(const QKVArgs& a, QKVP& k, cudaStream_t s, bool* handle
             vec = vec && (k.p.rot / 2) % N == 0 && aligned(a.cos, 16) && aligned(a.sin, 16);
         }
     }
-    if (!vec) return cudaSuccess;
     *handled = true;
-    const int lph = nvec;
-    const int hpw = 32 / lph;
-    const int threads = 256;
-    const int64_t per_block = (int64_t)(threads / 32) * hpw;
-    int64_t blocks = ((int64_t)k.p.units + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)sm_count() * (2048 / threads) * 64;
-    if (blocks > cap) blocks = cap;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -117,24 +158,57 @@ cudaError_t launch_typed(const QKVArgs& a, QKVP& k, cudaStream_t s, bool* handle
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    if (!vec) {
+        const int threads = 128;
+        int64_t blocks = ((int64_t)k.p.units + threads / 32 - 1) / (threads / 32);
+        const int64_t cap = (int64_t)sm_count() * 16;
+        if (blocks > cap) blocks = cap;
+        const size_t smem = (size_t)(threads / 32) * D * sizeof(float);
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(qkv_generic_kernel<T>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaLaunchKernelEx(&cfg, qkv_generic_kernel<T>, k, a.layout);
+    }
+    const int lph = nvec;
+    const int hpw = 32 / lph;
+    void (*vfn)(QKVP) = nullptr;
+    switch (lph) {
+        case 1: vfn = qkv_vec_fn<T, 1>(a.layout); break;
+        case 2: vfn = qkv_vec_fn<T, 2>(a.layout); break;
+        case 4: vfn = qkv_vec_fn<T, 4>(a.layout); break;
+        case 8: vfn = qkv_vec_fn<T, 8>(a.layout); break;
+        case 16: vfn = qkv_vec_fn<T, 16>(a.layout); break;
+        default: vfn = qkv_vec_fn<T, 32>(a.layout); break;
+    }
+    const int threads = 256;
+    const int64_t per_block = (int64_t)(threads / 32) * hpw;
+    int64_t blocks = ((int64_t)k.p.units + per_block - 1) / per_block;
+    // the prologue's rule: the one-shot lane-group grid while it fits in one
+    // wave of resident CTAs, four threads per head beyond
+    int path = qk_path_override();
+    if (path == 0) {
+        const int64_t wave = (int64_t)resident_ctas((const void*)vfn, threads) * sm_count();
+        path = blocks > wave && quad_suits(a.layout, k.p.rot, (int64_t)D * (int64_t)sizeof(T))
+                   ? 3
+                   : 1;
+    }
+    if (path == 3) {
+        bool quad = false;
+        cudaError_t e = launch_qkv_quad<T>(a, k, cfg, &quad);
+        if (quad || e != cudaSuccess) return e;
+    }
+    const int64_t cap = (int64_t)sm_count() * (2048 / threads) * 64;
+    if (blocks > cap) blocks = cap;
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(threads);
-#define EDGE_QKV_CASE(L)                                                                  \
-    case L:                                                                                \
-        return a.layout == kInterleaved ? cudaLaunchKernelEx(&cfg, qkv_vec_kernel<T, L, kInterleaved>, k) \
-                                        : cudaLaunchKernelEx(&cfg, qkv_vec_kernel<T, L, kRotateHalf>, k);
-    switch (lph) {
-        EDGE_QKV_CASE(1)
-        EDGE_QKV_CASE(2)
-        EDGE_QKV_CASE(4)
-        EDGE_QKV_CASE(8)
-        EDGE_QKV_CASE(16)
-        EDGE_QKV_CASE(32)
-        default: break;
-    }
-#undef EDGE_QKV_CASE
-    *handled = false;
-    return cudaSuccess;
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, vfn, k);
 }
 
 }  // namespace

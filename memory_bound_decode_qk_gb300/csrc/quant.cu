@@ -20,6 +20,12 @@ template <typename T>
 __global__ void __launch_bounds__(256) quant_kernel(const char* x, uint8_t* out, int64_t n,
                                                     int64_t nvec, float inv) {
     constexpr int N = vec_elems<T>();
+    if (threadIdx.x == 0 && nvec > 0) {
+        // this CTA's first vectors into L2 while the preceding grid drains
+        const int64_t v0 = (int64_t)blockIdx.x * blockDim.x;
+        const int64_t v1 = v0 + blockDim.x < nvec ? v0 + blockDim.x : nvec;
+        prefetch_l2(x, 16 * v0, 16 * v1);
+    }
     pdl_wait();
     pdl_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;

@@ -51,6 +51,15 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
     const int64_t in_row = (int64_t)p.hidden * (int64_t)sizeof(T);
     const int64_t out_row = FP8 ? (int64_t)p.hidden : in_row;
 
+    if (threadIdx.x == 0) {
+        // this CTA's first rows, and the weight (CTA 0), into L2 while the
+        // preceding grid drains
+        const int64_t r0 = (int64_t)blockIdx.x * p.RPB;
+        const int64_t r1 = r0 + p.RPB < p.rows ? r0 + p.RPB : p.rows;
+        prefetch_l2(p.x, r0 * in_row, r1 * in_row);
+        if (ADD) prefetch_l2(p.res, r0 * in_row, r1 * in_row);
+        if (blockIdx.x == 0) prefetch_l2(p.w, 0, in_row);
+    }
     pdl_wait();
     pdl_launch_dependents();
 
@@ -186,13 +195,30 @@ __device__ __forceinline__ float row_sum(float v, const RowsP& p, int g, int lan
     return v;
 }
 
+// row_sum with one barrier: the partial sums go to `buf`, which the caller
+// alternates between two reductions, so a buffer is rewritten only after a
+// later barrier that every reader of its previous contents has passed.
+__device__ __forceinline__ float row_sum_alt(float v, const RowsP& p, int g, int lane, int wib,
+                                             float* buf) {
+    v = group_sum<32>(v);
+    if (p.W > 1) {
+        if (lane == 0) buf[wib] = v;
+        __syncthreads();
+        v = 0.0f;
+        for (int k = 0; k < p.W; ++k) v = __fadd_rn(v, buf[g * p.W + k]);
+    }
+    return v;
+}
+
 // One-read LayerNorm (FlashRT siglip_layernorm_1read): the row stays in
 // registers for the mean, the variance of the centred values and the
-// output, so x is read from HBM once.  y = (x - mu) r gamma + beta.
+// output, so x is read from HBM once.  y = (x - mu) r gamma + beta.  gamma
+// and beta are loaded after the two reductions, so they hold no registers
+// across them.
 template <typename T, bool FP8, int V>
 __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
     constexpr int N = vec_elems<T>();
-    __shared__ float red[16];
+    __shared__ float red_mu[16], red_var[16];
     const int tpr = 32 * p.W;
     const int g = threadIdx.x / tpr;
     const int tid = threadIdx.x - g * tpr;
@@ -203,6 +229,15 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
     const uint4* gv = reinterpret_cast<const uint4*>(p.w);
     const uint4* bv = reinterpret_cast<const uint4*>(p.beta);
 
+    if (threadIdx.x == 0) {
+        const int64_t r0 = (int64_t)blockIdx.x * p.RPB;
+        const int64_t r1 = r0 + p.RPB < p.rows ? r0 + p.RPB : p.rows;
+        prefetch_l2(p.x, r0 * in_row, r1 * in_row);
+        if (blockIdx.x == 0) {
+            prefetch_l2(p.w, 0, in_row);
+            prefetch_l2(p.beta, 0, in_row);
+        }
+    }
     pdl_wait();
     pdl_launch_dependents();
 
@@ -210,14 +245,12 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
         const int64_t row = r0 + g;
         const bool active = row < p.rows;
         const uint4* xr = reinterpret_cast<const uint4*>(p.x + (active ? row : r0) * in_row);
-        uint4 xv[V], gr[V], br[V];
+        uint4 xv[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int idx = tid + i * tpr;
             const bool ok = active && idx < p.nvec;
             xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
-            gr[i] = (ok && gv != nullptr) ? __ldg(gv + idx) : make_uint4(0u, 0u, 0u, 0u);
-            br[i] = (ok && bv != nullptr) ? __ldg(bv + idx) : make_uint4(0u, 0u, 0u, 0u);
         }
         float sum = 0.0f;
 #pragma unroll
@@ -227,7 +260,7 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
 #pragma unroll
             for (int e = 0; e < N; ++e) sum = __fadd_rn(sum, a[e]);
         }
-        const float mu = __fmul_rn(row_sum(sum, p, g, lane, wib, red), p.invH);
+        const float mu = __fmul_rn(row_sum_alt(sum, p, g, lane, wib, red_mu), p.invH);
         float sq = 0.0f;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
@@ -241,7 +274,16 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
                 sq = __fmaf_rn(d, d, sq);
             }
         }
-        const float r = inv_rms(row_sum(sq, p, g, lane, wib, red), p.invH, p.eps);
+        const float r = inv_rms(row_sum_alt(sq, p, g, lane, wib, red_var), p.invH, p.eps);
+        // gamma and beta (L1/L2-resident), all issued before the output loop
+        uint4 gr[V], br[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int idx = tid + i * tpr;
+            const bool ok = active && idx < p.nvec;
+            gr[i] = (ok && gv != nullptr) ? __ldg(gv + idx) : make_uint4(0u, 0u, 0u, 0u);
+            br[i] = (ok && bv != nullptr) ? __ldg(bv + idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int idx = tid + i * tpr;
@@ -331,6 +373,9 @@ bool vec_shape(const RowsArgs& a, int sms, RowsP& p, int& V) {
     // target vectors per thread (measured on GB300: 1 for few rows, 2 for
     // many; more per thread lowers occupancy and loses bandwidth)
     int vt = a.rows >= 2 * sms ? 2 : 1;
+    // one input stream per row (plain RMSNorm): more vectors per thread keep
+    // enough bytes in flight once there are many rows (measured on GB300)
+    if (!a.residual && !a.layernorm && a.rows >= 8 * sms) vt = 4;
     if (rows_vt_override() > 0) vt = rows_vt_override();
     int W = (int)((nvec + 32 * vt - 1) / (32 * vt));
     if (W > 16) W = 16;

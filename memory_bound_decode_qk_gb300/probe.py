@@ -21,7 +21,7 @@ DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 
 
 def make_case(op, dtype, T, hq=16, hk=2, d=256, rot=64, hidden=2048, inter=9728, fp8=False,
-              layout=0, weight=True, device="cuda"):
+              layout=0, weight=True, device="cuda"):  # noqa: C901 (one branch per op)
     """A zero-argument callable that launches the op once on fresh buffers."""
     if op == "qk":
         i = synth.qk_inputs(0, dtype, T, hq, hk, d, rot, theta=1e7, cache_len=32768,
@@ -33,6 +33,14 @@ def make_case(op, dtype, T, hq=16, hk=2, d=256, rot=64, hidden=2048, inter=9728,
                                         t["cos"], t["sin"], rotary_dim=rot, layout=layout,
                                         weight_offset=1, q_out=qo, k_out=ko, fp8=fp8,
                                         inv_scale=40.0)
+    if op == "qk_dflash2":
+        # DFlash2 pair: 32 + 32 heads of 128, full rotary, direct weights, in place
+        i = synth.qk_inputs(0, dtype, T, 32, 32, 128, 128, theta=1e6, cache_len=32768,
+                            positions="blocks:16", w_mean=1.0, w_std=0.02)
+        t = {k: v.to(device) for k, v in i.items()}
+        return lambda: ops.qk_norm_rope(t["q"], t["k"], t["wq"], t["wk"], t["positions"],
+                                        t["cos"], t["sin"], rotary_dim=128, q_out=t["q"],
+                                        k_out=t["k"])
     if op in ("add_rmsnorm", "rmsnorm"):
         i = synth.rows_inputs(0, dtype, T, hidden, residual=op == "add_rmsnorm")
         x = i["x"].to(device)
@@ -42,6 +50,34 @@ def make_case(op, dtype, T, hq=16, hk=2, d=256, rot=64, hidden=2048, inter=9728,
             return lambda: ops.rmsnorm(x, w, out=o, fp8=fp8, inv_scale=40.0)
         r = i["residual"].to(device)
         return lambda: ops.add_rmsnorm(x, r, w, out=o, fp8=fp8, inv_scale=40.0)
+    if op == "rope":
+        i = synth.qk_inputs(0, dtype, T, hq, hk, d, rot, theta=1e7, cache_len=32768,
+                            positions="offset")
+        t = {k: (v.to(device) if v is not None else None) for k, v in i.items()}
+        qo, ko = torch.empty_like(t["q"]), torch.empty_like(t["k"])
+        return lambda: ops.rope(t["q"], t["k"], t["positions"], t["cos"], t["sin"],
+                                rotary_dim=rot, layout=layout, q_out=qo, k_out=ko)
+    if op == "layernorm":
+        i = synth.rows_inputs(0, dtype, T, hidden, residual=False)
+        x, g = i["x"].to(device), i["w"].to(device)
+        o = torch.empty(T, hidden, dtype=torch.uint8 if fp8 else dtype, device=device)
+        return lambda: ops.layernorm(x, g, g, out=o, fp8=fp8, inv_scale=40.0)
+    if op == "quantize":
+        x = synth.rows_inputs(0, dtype, T, hidden, residual=False)["x"].to(device)
+        o = torch.empty(x.shape, dtype=torch.uint8, device=device)
+        return lambda: ops.quantize_fp8(x, 40.0, out=o)
+    if op == "qkv_cache":
+        qkv = synth.to_dtype(synth.normal(0, 71, T * (hq + 2 * hk) * d), dtype).view(T, -1)
+        qkv = qkv.to(device)
+        w = synth.to_dtype(synth.normal(0, 72, d, 0.0, 0.05), dtype).to(device)
+        cos, sin = synth.rope_cache(1e7, rot, 32768)
+        cos, sin = cos.to(device), sin.to(device)
+        pos = torch.arange(T, dtype=torch.int64, device=device)
+        kc = torch.empty(T, hk, d, dtype=dtype, device=device)
+        vc = torch.empty_like(kc)
+        qo = torch.empty(T, hq, d, dtype=dtype, device=device)
+        return lambda: ops.qkv_rope_cache(qkv, hq, hk, w, w, pos, cos, sin, pos, kc, vc,
+                                          rotary_dim=rot, weight_offset=1, q_out=qo)
     if op in ("glu_silu", "glu_gelu"):
         gu = synth.glu_inputs(0, dtype, T, inter)["gate_up"].to(device)
         o = torch.empty(T, inter, dtype=torch.uint8 if fp8 else dtype, device=device)
@@ -60,13 +96,19 @@ SWEEP = (
     + [("rmsnorm", dict(T=T, hidden=2048, fp8=True, weight=False)) for T in (64, 512, 4096)]
     + [("glu_silu", dict(T=T, inter=9728)) for T in (1, 64, 512, 4096)]
     + [("glu_gelu", dict(T=T, inter=2048, fp8=True)) for T in (64, 512, 4096)]
+    + [("qk_dflash2", dict(T=16 * B)) for B in (1, 16, 64)]
+    + [("rope", dict(T=T, hq=24, hk=4)) for T in (1, 512, 2048)]
+    + [("layernorm", dict(T=T, hidden=1152)) for T in (1, 512, 4096)]
+    + [("quantize", dict(T=T, hidden=2048)) for T in (512, 4096)]
+    + [("qkv_cache", dict(T=T, hq=16, hk=2)) for T in (1, 512, 2048)]
 )
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", default="qk", choices=["qk", "add_rmsnorm", "rmsnorm", "glu_silu",
-                                                   "glu_gelu"])
+                                                   "glu_gelu", "rope", "layernorm", "quantize",
+                                                   "qkv_cache", "qk_dflash2"])
     ap.add_argument("--dtype", default="bf16", choices=list(DT))
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--hq", type=int, default=16)

@@ -97,13 +97,22 @@ S_GU = 21
 S_OUT_X, S_OUT_RES, S_OUT_GU = 31, 32, 33
 
 
+def block_positions(seed: int, W: int, B: int, cache_len: int) -> np.ndarray:
+    """Positions of B sequences of W consecutive tokens each, tokens ordered
+    [B][W]: sequence b starts at a seeded offset in [0, cache_len - W]."""
+    u = uniform(seed, S_POS, max(B, 1))
+    off = np.floor(u[:B] * (cache_len - W + 1)).astype(np.int64)
+    return (off[:, None] + np.arange(W, dtype=np.int64)[None, :]).reshape(-1)
+
+
 def qk_inputs(seed, dtype, T, Hq, Hk, D, rotary_dim, *, theta, cache_len, positions,
               w_mean=0.0, w_std=0.1, x_std=1.0):
     """Inputs of the fused QK prologue.
 
     positions: an int64 array of length T, or one of "cfg_out_of_cache"
     (uniform in [0, cache_len) with the last token at cache_len), "offset"
-    (a seeded offset in [0, cache_len - T] plus 0..T-1) or "arange" (0..T-1).
+    (a seeded offset in [0, cache_len - T] plus 0..T-1), "arange" (0..T-1) or
+    "blocks:W" (T // W sequences of W consecutive tokens, block_positions).
     """
     q = to_dtype(normal(seed, S_Q, T * Hq * D, 0.0, x_std), dtype).view(T, Hq, D)
     k = to_dtype(normal(seed, S_K, T * Hk * D, 0.0, x_std), dtype).view(T, Hk, D)
@@ -120,6 +129,11 @@ def qk_inputs(seed, dtype, T, Hq, Hk, D, rotary_dim, *, theta, cache_len, positi
             pos = off + np.arange(T, dtype=np.int64)
         elif positions == "arange":
             pos = np.arange(T, dtype=np.int64)
+        elif positions.startswith("blocks:"):
+            W = int(positions.split(":", 1)[1])
+            if W <= 0 or T % W:
+                raise ValueError(positions)
+            pos = block_positions(seed, W, T // W, cache_len)
         else:
             raise ValueError(positions)
     else:

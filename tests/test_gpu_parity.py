@@ -158,19 +158,35 @@ QK_CASES = {
                         w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=16, positions="arange"),
     "no_weight": dict(dtype=torch.bfloat16, T=4, Hq=8, Hk=2, D=256, rot=64, layout=0,
                       w_mean=None, w_std=0.0, offset=0, theta=1e7, P=64, positions="arange"),
-    # many heads (>= 128 per SM): the four-threads-per-head path
+    # DFlash2 pair [128, 32, W, B] (innermost first): q and k both 32 heads of
+    # 128, in place, direct weights, full rotate-half rotary; B sequences of W
+    # consecutive draft positions.  W*B = 64 runs the lane-group path, 512 the
+    # four-threads-per-head path, 21 a ragged block count.
+    "dflash2_W16_B4": dict(dtype=torch.bfloat16, T=64, Hq=32, Hk=32, D=128, rot=128, layout=0,
+                           w_mean=1.0, w_std=0.02, offset=0, theta=1e6, P=32768,
+                           positions="blocks:16", inplace=True),
+    "dflash2_W16_B32": dict(dtype=torch.bfloat16, T=512, Hq=32, Hk=32, D=128, rot=128, layout=0,
+                            w_mean=1.0, w_std=0.02, offset=0, theta=1e6, P=32768,
+                            positions="blocks:16", inplace=True),
+    "dflash2_W7_B3": dict(dtype=torch.bfloat16, T=21, Hq=32, Hk=32, D=128, rot=128, layout=0,
+                          w_mean=1.0, w_std=0.02, offset=0, theta=1e6, P=32768,
+                          positions="blocks:7", inplace=True),
+    # many heads (the lane-group grid is over a wave of resident CTAs): the
+    # four-threads-per-head path
     "quad_f32_d128": dict(dtype=torch.float32, T=2001, Hq=8, Hk=2, D=128, rot=128, layout=0,
                           w_mean=0.0, w_std=0.1, offset=1, theta=1e6, P=4096,
                           positions=np.r_[np.arange(1999), [4096, -3]]),
-    "quad_f16_d64_interleaved": dict(dtype=torch.float16, T=2500, Hq=4, Hk=4, D=64, rot=32,
+    "quad_f16_d64_interleaved": dict(dtype=torch.float16, T=6000, Hq=4, Hk=4, D=64, rot=32,
                                      layout=1, w_mean=0.0, w_std=0.1, offset=1, theta=1e4,
                                      P=4096, positions="arange"),
-    "quad_bf16_d128_no_k": dict(dtype=torch.bfloat16, T=650, Hq=32, Hk=0, D=128, rot=128,
+    "quad_bf16_d128_no_k": dict(dtype=torch.bfloat16, T=1700, Hq=32, Hk=0, D=128, rot=128,
                                 layout=0, w_mean=1.0, w_std=0.02, offset=0, theta=1e6,
                                 P=4096, positions="offset", inplace=True),
     "quad_no_weight": dict(dtype=torch.bfloat16, T=700, Hq=24, Hk=4, D=256, rot=64, layout=0,
                            w_mean=None, w_std=0.0, offset=0, theta=1e7, P=32768,
                            positions="offset"),
+    # interleaved 512-byte heads with rotation stay on the lane-group path at
+    # every width (the dispatch), here at many heads
     "quad_cfg4_interleaved": dict(dtype=torch.bfloat16, T=1000, Hq=16, Hk=8, D=256, rot=256,
                                   layout=1, w_mean=1.0, w_std=0.02, offset=0, theta=1e6,
                                   P=4096, positions="arange", inplace=True),
@@ -241,12 +257,24 @@ def test_qk_norm_rope(name):
 
 @pytest.mark.parametrize("name", ["cfg3_16_2_T333", "cfg3_24_4_T8", "cfg4_bf16", "cfg1_f32",
                                   "generic_odd_d37", "d128_bf16", "quad_f32_d128",
-                                  "quad_f16_d64_interleaved", "quad_cfg4_interleaved"])
+                                  "quad_f16_d64_interleaved", "quad_cfg4_interleaved",
+                                  "dflash2_W16_B32"])
 def test_qk_norm_rope_fp8(name):
     c = dict(QK_CASES[name])
     ref, gq, gk, fmt, out_fmt, inv = run_qk(c, fp8=True)
     check_fp8_out(name + " q", gq, ref.q_lo, ref.q_hi, ref.q_mag, ETA_NORM, inv)
     check_fp8_out(name + " k", gk, ref.k_lo, ref.k_hi, ref.k_mag, ETA_NORM, inv)
+
+
+@pytest.mark.parametrize("T", [16, 1024])
+def test_qk_dflash2_full_size(T):
+    # the DFlash2 pair at the benchmark's block sizes (W = 16; B = 1 and 64)
+    c = dict(QK_CASES["dflash2_W16_B4"], T=T)
+    ref, gq, gk, fmt, out_fmt, _ = run_qk(c)
+    check_out("q", gq, ref.q_out, ref.q_pre, ref.q_mag, fmt, out_fmt, ETA_NORM, lo=ref.q_lo,
+              hi=ref.q_hi)
+    check_out("k", gk, ref.k_out, ref.k_pre, ref.k_mag, fmt, out_fmt, ETA_NORM, lo=ref.k_lo,
+              hi=ref.k_hi)
 
 
 @pytest.mark.parametrize("geom", [(16, 2), (24, 4)])
@@ -666,6 +694,28 @@ QKV_CASES = {
                       offset=1, S=4),
     "prefill_T2000": dict(dtype=torch.bfloat16, T=2000, Hq=16, Hk=2, D=256, rot=64, layout=0,
                           norm=True, offset=1, S=2048),
+    # many heads (the lane-group grid is over a wave): four threads per head
+    "quad_qwen_d128_T1000": dict(dtype=torch.bfloat16, T=1000, Hq=32, Hk=8, D=128, rot=128,
+                                 layout=0, norm=True, offset=0, S=1024),
+    "quad_f16_interleaved_d128": dict(dtype=torch.float16, T=700, Hq=16, Hk=4, D=128, rot=64,
+                                      layout=1, norm=True, offset=1, S=700),
+    "quad_f32_d64_no_norm": dict(dtype=torch.float32, T=2000, Hq=8, Hk=2, D=64, rot=64, layout=0,
+                                 norm=False, offset=0, S=2000),
+    "quad_no_cache_T1500": dict(dtype=torch.bfloat16, T=1500, Hq=16, Hk=2, D=256, rot=64,
+                                layout=0, norm=True, offset=1, S=0),
+    # no cache given (kv_heads > 0, num_slots 0, slots and caches NULL): q only
+    "no_cache": dict(dtype=torch.bfloat16, T=12, Hq=8, Hk=2, D=128, rot=128, layout=0,
+                     norm=True, offset=1, S=0),
+    # the scalar path: head sizes that are no power-of-two number of vectors,
+    # odd sizes, ragged rotary, misaligned tensors
+    "generic_d96": dict(dtype=torch.bfloat16, T=7, Hq=4, Hk=1, D=96, rot=96, layout=0, norm=True,
+                        offset=1, S=8),
+    "generic_odd_d37_f16": dict(dtype=torch.float16, T=6, Hq=3, Hk=2, D=37, rot=20, layout=1,
+                                norm=True, offset=0, S=7),
+    "generic_f32_rot24": dict(dtype=torch.float32, T=5, Hq=4, Hk=2, D=256, rot=24, layout=0,
+                              norm=False, offset=0, S=6),
+    "generic_misaligned": dict(dtype=torch.bfloat16, T=9, Hq=16, Hk=2, D=256, rot=64, layout=0,
+                               norm=True, offset=1, S=16, misalign=1),
 }
 
 
@@ -679,7 +729,9 @@ def run_qkv(c):
     cos, sin = synth.rope_cache(1e6, c["rot"], P)
     pos = np.floor(synth.uniform(0, 74, T) * P).astype(np.int64)
     pos[T // 3] = P            # out of cache: normalized, not rotated
-    slots = np.arange(T, dtype=np.int64) % S
+    # distinct slots (two tokens on one slot leave either row: unspecified)
+    assert S == 0 or T <= S, "the case needs a slot per token"
+    slots = np.arange(T, dtype=np.int64) % max(S, 1) if S else np.full(T, -1, np.int64)
     if T > 2:
         slots[1] = -1          # padding token: no cache write
         slots[2] = S + 5       # out of range: no cache write
@@ -688,15 +740,27 @@ def run_qkv(c):
     ref = oracle.qkv_rope_cache(storage(qkv), storage(wq), storage(wk), fmt, Hq, Hk, c["rot"],
                                 c["layout"], pos, storage(cos), storage(sin), slots, storage(kc0),
                                 storage(vc0), 1e-6, c["offset"], c["norm"], eta=ETA_NORM)
-    kc = Guarded((S, Hk, D), dtype)
-    vc = Guarded((S, Hk, D), dtype)
+    mis = c.get("misalign", 0)
+    qo = Guarded((T, Hq, D), dtype, mis)
+    if S == 0:
+        edge_ops.qkv_rope_cache(dev(qkv, mis), Hq, Hk, dev(wq, mis), dev(wk, mis),
+                                dev(torch.from_numpy(pos)), dev(cos), dev(sin), None, None, None,
+                                rotary_dim=c["rot"], layout=c["layout"], eps=1e-6,
+                                weight_offset=c["offset"], normalize=c["norm"], q_out=qo.t)
+        torch.cuda.synchronize()
+        qo.check()
+        check_out("q", storage(qo.t.cpu()), ref.q_out, ref.q_pre, ref.q_mag, fmt, fmt, ETA_NORM,
+                  lo=ref.q_lo, hi=ref.q_hi)
+        return
+    kc = Guarded((S, Hk, D), dtype, mis)
+    vc = Guarded((S, Hk, D), dtype, mis)
     kc.t.copy_(kc0)
     vc.t.copy_(vc0)
-    qo = Guarded((T, Hq, D), dtype)
-    edge_ops.qkv_rope_cache(dev(qkv), Hq, Hk, dev(wq), dev(wk), dev(torch.from_numpy(pos)),
-                            dev(cos), dev(sin), dev(torch.from_numpy(slots)), kc.t, vc.t,
-                            rotary_dim=c["rot"], layout=c["layout"], eps=1e-6,
-                            weight_offset=c["offset"], normalize=c["norm"], q_out=qo.t)
+    edge_ops.qkv_rope_cache(dev(qkv, mis), Hq, Hk, dev(wq, mis), dev(wk, mis),
+                            dev(torch.from_numpy(pos)), dev(cos), dev(sin),
+                            dev(torch.from_numpy(slots)), kc.t, vc.t, rotary_dim=c["rot"],
+                            layout=c["layout"], eps=1e-6, weight_offset=c["offset"],
+                            normalize=c["norm"], q_out=qo.t)
     torch.cuda.synchronize()
     for g in (kc, vc, qo):
         g.check()
@@ -717,13 +781,3 @@ def run_qkv(c):
 @pytest.mark.parametrize("name", list(QKV_CASES))
 def test_qkv_rope_cache(name):
     run_qkv(QKV_CASES[name])
-
-
-def test_qkv_rope_cache_unsupported_shape_launches_nothing():
-    qkv = torch.zeros(2, 4 * 96, dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros(4, 1, 96, dtype=torch.bfloat16, device="cuda")
-    vc = torch.zeros_like(kc)
-    slots = torch.zeros(2, dtype=torch.int64, device="cuda")
-    with pytest.raises(edge_ops.EdgeError, match="UNSUPPORTED"):
-        edge_ops.qkv_rope_cache(qkv, 2, 1, None, None, None, None, None, slots, kc, vc,
-                                rotary_dim=0)

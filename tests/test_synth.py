@@ -1,6 +1,7 @@
 """The seeded generator is deterministic, stream-separated and has the
 requested distributions."""
 import numpy as np
+import pytest
 import torch
 
 from memory_bound_decode_qk_gb300 import synth
@@ -54,3 +55,21 @@ def test_rope_cache_rows():
     cos, sin = synth.rope_cache(1e4, 8, 3)
     assert torch.equal(cos[0], torch.ones(4)) and torch.equal(sin[0], torch.zeros(4))
     np.testing.assert_allclose(cos[2, 1].item(), np.cos(2 * 1e4 ** (-2 / 8)), rtol=1e-7)
+
+
+def test_block_positions():
+    # B sequences of W consecutive positions, each inside the cache, ordered [B][W]
+    p = synth.block_positions(0, 16, 5, 32768)
+    assert p.shape == (80,) and p.dtype == np.int64
+    blocks = p.reshape(5, 16)
+    assert np.all(np.diff(blocks, axis=1) == 1)
+    assert blocks[:, 0].min() >= 0 and blocks[:, -1].max() < 32768
+    assert len(set(blocks[:, 0].tolist())) > 1
+    # W equal to the cache length leaves a single start, 0
+    assert np.array_equal(synth.block_positions(3, 8, 2, 8), np.tile(np.arange(8), 2))
+    inp = synth.qk_inputs(0, torch.bfloat16, 48, 2, 2, 128, 128, theta=1e6, cache_len=4096,
+                          positions="blocks:16")
+    assert np.array_equal(inp["positions"].numpy(), synth.block_positions(0, 16, 3, 4096))
+    with pytest.raises(ValueError):
+        synth.qk_inputs(0, torch.bfloat16, 50, 2, 2, 128, 128, theta=1e6, cache_len=4096,
+                        positions="blocks:16")

@@ -89,6 +89,15 @@ int rows_vt_override() {
     return v;
 }
 
+int ln_warp_override() {
+    static const int v = [] {
+        const char* e = std::getenv("EDGE_OPS_LN_WARP");
+        if (e == nullptr || (e[0] != '0' && e[0] != '1') || e[1] != 0) return -1;
+        return e[0] - '0';
+    }();
+    return v;
+}
+
 int glu_unroll_override() {
     static const int v = env_choice("EDGE_OPS_GLU_UNROLL", {1, 2, 4});
     return v;

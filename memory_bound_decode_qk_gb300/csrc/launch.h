@@ -109,6 +109,9 @@ bool pdl_enabled();
 int qk_path_override();
 int rows_vt_override();
 int glu_unroll_override();
+// EDGE_OPS_LN_WARP: 1 one warp per LayerNorm row, 0 never; -1 (unset) the
+// built-in choice.
+int ln_warp_override();
 
 
 }  // namespace edge

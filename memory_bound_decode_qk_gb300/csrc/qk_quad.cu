@@ -50,12 +50,26 @@ constexpr int K = 4;  // threads per head
 // thread.  Measured on GB300: those 16-bit heads ran faster at 2 CTAs than at
 // 3 with spills, while fp32 512-byte heads (32 elements per thread) ran
 // faster at 3 CTAs, spilling about a hundred bytes, than at 2.
-template <typename T, bool FP8, int C, int LAYOUT, int RQ>
-constexpr int quad_min_blocks() {
+// With PIPE a thread holds two heads' chunks, so each size steps down one
+// CTA count: 4 for 128-byte heads, 3 for 256-byte heads, 2 for 512-byte heads.
+template <typename T, bool FP8, int C, int LAYOUT, int RQ, bool PIPE>
+__host__ __device__ constexpr int quad_min_blocks() {
     return FP8 ? 2
-               : C <= 2 ? 5
-               : C <= 4 ? 4
-               : (sizeof(T) == 2 && (LAYOUT == kInterleaved || 2 * RQ > 2)) ? 2 : 3;
+           : PIPE ? (C <= 2 ? 4 : C <= 4 ? 3 : 2)
+                  : C <= 2 ? 5
+                  : C <= 4 ? 4
+                  : (sizeof(T) == 2 && (LAYOUT == kInterleaved || 2 * RQ > 2)) ? 2 : 3;
+}
+
+// Which variants run the resident, load-ahead form.  Measured on GB300 at
+// T = 1024 to 4096: 10-24% faster for 512-byte heads with at most two
+// rotate-half chunks per thread (the text profiles, fp32 heads of 128),
+// slower for 256-byte heads (whose one-pass form already holds 4 CTAs per SM)
+// and no faster for 16-bit 512-byte heads that are interleaved or rotate
+// fully (whose one-pass form already runs at 2 CTAs).
+template <typename T, int C, int LAYOUT, int RQ>
+__host__ __device__ constexpr bool quad_pipe() {
+    return C == 8 && !(sizeof(T) == 2 && (LAYOUT == kInterleaved || 2 * RQ > 2));
 }
 
 constexpr int kKindQ = 0, kKindK = 1, kKindV = 2;
@@ -120,9 +134,21 @@ struct QKVMap {
     }
 };
 
+// One head unit's loaded chunks and what the arithmetic needs besides them.
+template <int C>
+struct QuadHead {
+    uint4 raw[C];
+    QuadUnit un;
+    int64_t pos;
+    bool active, isv;
+};
+
 // RQ: rotate-half: chunks per thread that are first members (HVQ); interleaved:
 // chunks per thread that rotate.  0: no channel rotates.
-template <typename T, bool FP8, int C, int LAYOUT, int RQ, class Map>
+// PIPE: a resident grid in which every thread issues its next head's loads
+// before the arithmetic of the current one, so that memory and arithmetic
+// overlap across iterations instead of alternating in lockstep waves.
+template <typename T, bool FP8, int C, int LAYOUT, int RQ, bool PIPE, class Map>
 __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
     constexpr int N = vec_elems<T>();
     constexpr int D = C * K * N;
@@ -137,35 +163,49 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
     pdl_wait();
     pdl_launch_dependents();
 
-    for (int e = threadIdx.x; e < D; e += blockDim.x) {
-        const float dq = p.wq ? __fadd_rn(to_f(reinterpret_cast<const T*>(p.wq)[e]), p.delta) : 1.0f;
-        const float dk = p.wk ? __fadd_rn(to_f(reinterpret_cast<const T*>(p.wk)[e]), p.delta) : 1.0f;
-        wsm[kKindQ][e] = dq;
-        wsm[kKindK][e] = dk;
-        wsm[kKindV][e] = 1.0f;
-    }
-    __syncthreads();
-
     const int kt = threadIdx.x & (K - 1);
     const int hs = threadIdx.x / K;           // head slot in the CTA
     const uint32_t hb = (uint32_t)D * sizeof(T);
+    const uint32_t stride = gridDim.x * heads_per_cta;
 
-    for (uint32_t base = blockIdx.x * heads_per_cta; base < p.units;
-         base += gridDim.x * heads_per_cta) {
+    // The weights are staged while the first heads are in flight in the
+    // prologue (measured 3-10% faster on GB300), and before the first heads in
+    // the fused QKV op, whose value-head bookkeeping leaves no registers for
+    // the overlap (measured 7% faster that way).
+    auto stage = [&]() {
+        for (int e = threadIdx.x; e < D; e += blockDim.x) {
+            const float dq =
+                p.wq ? __fadd_rn(to_f(reinterpret_cast<const T*>(p.wq)[e]), p.delta) : 1.0f;
+            const float dk =
+                p.wk ? __fadd_rn(to_f(reinterpret_cast<const T*>(p.wk)[e]), p.delta) : 1.0f;
+            wsm[kKindQ][e] = dq;
+            wsm[kKindK][e] = dk;
+            wsm[kKindV][e] = 1.0f;
+        }
+        __syncthreads();
+    };
+
+    // issue every load of the unit in slot hs of the pass at `base`
+    auto load = [&](uint32_t base, QuadHead<C>& h) {
         const uint32_t u = base + hs;
-        const bool active = u < p.units;
-        const QuadUnit un = map.unit(p, active ? u : base, hb);
-
-        uint4 raw[C];
+        h.active = u < p.units;
+        h.un = map.unit(p, h.active ? u : base, hb);
 #pragma unroll
         for (int i = 0; i < C; ++i) {
-            raw[i] = active ? __ldcs(reinterpret_cast<const uint4*>(un.src) + kt + K * i)
-                            : make_uint4(0u, 0u, 0u, 0u);
+            h.raw[i] = h.active ? __ldcs(reinterpret_cast<const uint4*>(h.un.src) + kt + K * i)
+                                : make_uint4(0u, 0u, 0u, 0u);
         }
-        const bool isv = Map::kHasV && un.kind == kKindV;
-        int64_t pos = -1;
-        if (RQ > 0 && active && !isv) pos = __ldg(p.pos + un.t);
+        h.isv = Map::kHasV && h.un.kind == kKindV;
+        h.pos = -1;
+        if (RQ > 0 && h.active && !h.isv) h.pos = __ldg(p.pos + h.un.t);
+    };
 
+    // the arithmetic and stores of one loaded unit
+    auto process = [&](QuadHead<C>& h) {
+        uint4 (&raw)[C] = h.raw;
+        const QuadUnit& un = h.un;
+        const bool active = h.active, isv = h.isv;
+        const int64_t pos = h.pos;
         float ss = 0.0f;
 #pragma unroll
         for (int i = 0; i < C; ++i) {
@@ -204,7 +244,7 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
         }
 
         const bool rot = RQ > 0 && pos >= 0 && pos < p.cache_len;
-        if (!active || (Map::kHasV && un.dst == nullptr)) continue;
+        if (!active || (Map::kHasV && un.dst == nullptr)) return;
         char* out = un.dst;
         auto emit = [&](int i, const float (&y)[N]) {
             if constexpr (FP8) {
@@ -286,19 +326,58 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
                 }
             }
         }
+    };
+
+    uint32_t base = blockIdx.x * heads_per_cta;
+    if (base >= p.units) return;  // the same for the whole CTA
+    if constexpr (Map::kHasV) stage();
+    QuadHead<C> h0;
+    load(base, h0);
+    if constexpr (!Map::kHasV) stage();
+    if constexpr (PIPE) {
+        // two buffers in turn: the next pass is loaded into one while the
+        // other is processed (passes are the same for the whole CTA)
+        QuadHead<C> h1;
+        for (;;) {
+            uint32_t next = base + stride;
+            if (next >= p.units) {
+                process(h0);
+                break;
+            }
+            load(next, h1);
+            process(h0);
+            base = next;
+            next = base + stride;
+            if (next >= p.units) {
+                process(h1);
+                break;
+            }
+            load(next, h0);
+            process(h1);
+            base = next;
+        }
+    } else {
+        for (;;) {
+            process(h0);
+            base += stride;
+            if (base >= p.units) break;
+            load(base, h0);
+        }
     }
 }
 
 template <typename T, bool FP8, int C, int LAYOUT, int RQ>
-__global__ void __launch_bounds__(256, (quad_min_blocks<T, FP8, C, LAYOUT, RQ>()))
+__global__ void __launch_bounds__(256, (quad_min_blocks<T, FP8, C, LAYOUT, RQ,
+                                                        quad_pipe<T, C, LAYOUT, RQ>()>()))
     qk_quad_kernel(QKP p) {
-    quad_body<T, FP8, C, LAYOUT, RQ>(p, QKMap{});
+    quad_body<T, FP8, C, LAYOUT, RQ, quad_pipe<T, C, LAYOUT, RQ>()>(p, QKMap{});
 }
 
 template <typename T, int C, int LAYOUT, int RQ>
-__global__ void __launch_bounds__(256, (quad_min_blocks<T, false, C, LAYOUT, RQ>()))
+__global__ void __launch_bounds__(256, (quad_min_blocks<T, false, C, LAYOUT, RQ,
+                                                        quad_pipe<T, C, LAYOUT, RQ>()>()))
     qkv_quad_kernel(QKVP a) {
-    quad_body<T, false, C, LAYOUT, RQ>(a.p, QKVMap{&a});
+    quad_body<T, false, C, LAYOUT, RQ, quad_pipe<T, C, LAYOUT, RQ>()>(a.p, QKVMap{&a});
 }
 
 // Kernel selectors for pick_rq: the prologue (FP8 or not) and the fused QKV op.
@@ -361,12 +440,19 @@ bool quad_shape(int head_dim, int rot, int layout, const void* const* bufs, int 
     return true;
 }
 
+// quad_pipe for run-time (C, layout, RQ)
+template <typename T>
+bool pipe_of(int C, int layout, int rq) {
+    return C == 8 && !(sizeof(T) == 2 && (layout == kInterleaved || 2 * rq > 2));
+}
+
 template <typename P, typename Fn>
-cudaError_t launch_quad(Fn fn, const P& arg, uint32_t units, cudaLaunchConfig_t cfg) {
+cudaError_t launch_quad(Fn fn, const P& arg, uint32_t units, bool pipe, cudaLaunchConfig_t cfg) {
     const int threads = 256;
     const int64_t per_block = threads / K;
     int64_t blocks = ((int64_t)units + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)sm_count() * 64;
+    // the load-ahead form needs every CTA resident for all its passes
+    const int64_t cap = (int64_t)sm_count() * (pipe ? resident_ctas((const void*)fn, threads) : 64);
     if (blocks > cap) blocks = cap;
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(threads);
@@ -399,7 +485,7 @@ cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg
     }
     if (fn == nullptr) return cudaSuccess;
     *handled = true;
-    return launch_quad(fn, p, p.units, cfg);
+    return launch_quad(fn, p, p.units, pipe_of<T>(C, a.layout, rq), cfg);
 }
 
 template <typename T>
@@ -419,7 +505,7 @@ cudaError_t launch_qkv_quad(const QKVArgs& a, const QKVP& k, cudaLaunchConfig_t 
     }
     if (fn == nullptr) return cudaSuccess;
     *handled = true;
-    return launch_quad(fn, k, k.p.units, cfg);
+    return launch_quad(fn, k, k.p.units, pipe_of<T>(C, a.layout, rq), cfg);
 }
 
 bool quad_suits(int layout, int rotary_dim, int64_t head_bytes) {

@@ -310,6 +310,119 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
     }
 }
 
+// LayerNorm with one warp per row, for rows of at most 256 16-byte vectors
+// (bf16/fp16 width <= 2048, fp32 <= 1024).  Both reductions are warp
+// shuffles, with no block barrier per row.  gamma and beta are staged once per
+// CTA in shared memory, so the output loop reads them without global latency
+// and they hold no registers across the reductions.  A lane holds
+// V = ceil(vectors / 32) <= 8 vectors, so few registers are live and many
+// rows are in flight per SM.
+// Register budget: 4 CTAs per SM (64 registers) up to 4 vectors per lane, 3
+// (85) at 5 and 2 (128) beyond, the counts at which ptxas for sm_103a keeps
+// the variants spill-free (the 16-bit FP8 ones at 4 vectors spill under 32
+// bytes).
+template <int V>
+constexpr int ln_warp_min_blocks() {
+    return V <= 4 ? 4 : V == 5 ? 3 : 2;
+}
+
+template <typename T, bool FP8, int V>
+__global__ void __launch_bounds__(256, ln_warp_min_blocks<V>()) ln_warp_kernel(RowsP p) {
+    constexpr int N = vec_elems<T>();
+    extern __shared__ __align__(16) uint4 ln_gb[];  // gamma [nvec], then beta [nvec]
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    const int64_t in_row = (int64_t)p.hidden * (int64_t)sizeof(T);
+    const int64_t out_row = FP8 ? (int64_t)p.hidden : in_row;
+    const uint4* gv = reinterpret_cast<const uint4*>(p.w);
+    const uint4* bv = reinterpret_cast<const uint4*>(p.beta);
+
+    if (threadIdx.x == 0) {
+        const int64_t r0 = (int64_t)blockIdx.x * wpb;
+        const int64_t r1 = r0 + wpb < p.rows ? r0 + wpb : p.rows;
+        prefetch_l2(p.x, r0 * in_row, r1 * in_row);
+        if (blockIdx.x == 0) {
+            prefetch_l2(p.w, 0, in_row);
+            prefetch_l2(p.beta, 0, in_row);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+
+    uint4* gs = ln_gb;
+    uint4* bs = ln_gb + p.nvec;
+    bool staged = false;
+    // passes over wpb rows at a time (the same for the whole CTA, so the one
+    // barrier below is reached by every warp)
+    for (int64_t base = (int64_t)blockIdx.x * wpb; base < p.rows; base += (int64_t)gridDim.x * wpb) {
+        const int64_t row = base + (threadIdx.x >> 5);
+        const bool active = row < p.rows;
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + (active ? row : base) * in_row);
+        uint4 xv[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int idx = lane + 32 * i;
+            xv[i] = (active && idx < p.nvec) ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (!staged) {
+            // gamma and beta into shared memory while the first rows are in
+            // flight
+            for (int i = threadIdx.x; i < p.nvec; i += blockDim.x) {
+                if (gv != nullptr) gs[i] = __ldg(gv + i);
+                if (bv != nullptr) bs[i] = __ldg(bv + i);
+            }
+            __syncthreads();
+            staged = true;
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float a[N];
+            unpack_vec<T, N>(xv[i], a);
+#pragma unroll
+            for (int e = 0; e < N; ++e) sum = __fadd_rn(sum, a[e]);
+        }
+        const float mu = __fmul_rn(group_sum<32>(sum), p.invH);
+        float sq = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            if (lane + 32 * i >= p.nvec) continue;  // padding lanes add nothing
+            float a[N];
+            unpack_vec<T, N>(xv[i], a);
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                const float d = __fsub_rn(a[e], mu);
+                sq = __fmaf_rn(d, d, sq);
+            }
+        }
+        const float r = inv_rms(group_sum<32>(sq), p.invH, p.eps);
+        if (!active) continue;
+        char* orow = p.out + row * out_row;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int idx = lane + 32 * i;
+            if (idx >= p.nvec) continue;
+            float a[N], gg[N], bb[N], y[N];
+            unpack_vec<T, N>(xv[i], a);
+            if (gv != nullptr) unpack_vec<T, N>(gs[idx], gg);
+            if (bv != nullptr) unpack_vec<T, N>(bs[idx], bb);
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                float v = __fmul_rn(__fsub_rn(a[e], mu), r);
+                if (gv != nullptr) v = __fmul_rn(v, gg[e]);
+                if (bv != nullptr) v = __fadd_rn(v, bb[e]);
+                y[e] = v;
+            }
+            if constexpr (FP8) {
+                auto q8 = quantize_vec<N>(y, p.inv);
+                reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
+            } else {
+                reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
+            }
+        }
+    }
+}
+
 // Any size or alignment: one CTA per row, three passes (the second and third
 // hit L1/L2).
 template <typename T, bool FP8>
@@ -401,6 +514,33 @@ cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
 
     int V = 1;
+    int ln_warp = ln_warp_override();
+    if (ln_warp < 0) {
+        // one warp per row once there are many rows.  Measured crossover on
+        // GB300: T = 768 at width 1152 (5 vectors per lane), T = 1536 at
+        // width 2048 (8 vectors per lane, fewer CTAs per SM)
+        const int64_t lanes_vecs = ((int64_t)a.hidden / vec_elems<T>() + 31) / 32;
+        ln_warp = a.rows >= (lanes_vecs <= 5 ? 5 : 10) * (int64_t)sms;
+    }
+    if (vec_shape<T, FP8>(a, sms, p, V) && a.layernorm && p.nvec <= 256 && ln_warp) {
+        const int threads = 256;
+        int64_t blocks = (a.rows + 7) / 8;
+        const int64_t cap = (int64_t)sms * 64;
+        if (blocks > cap) blocks = cap;
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = (size_t)2 * p.nvec * 16;
+        switch ((p.nvec + 31) / 32) {
+            case 1: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 1>, p);
+            case 2: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 2>, p);
+            case 3: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 3>, p);
+            case 4: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 4>, p);
+            case 5: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 5>, p);
+            case 6: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 6>, p);
+            case 7: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 7>, p);
+            default: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 8>, p);
+        }
+    }
     if (vec_shape<T, FP8>(a, sms, p, V)) {
         const int threads = 32 * p.W * p.RPB;
         int64_t blocks = (a.rows + p.RPB - 1) / p.RPB;

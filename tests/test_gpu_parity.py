@@ -621,6 +621,14 @@ LN_CASES = {
     "f16_h37_generic": dict(dtype=torch.float16, T=40, H=37, affine=True),
     "bf16_h1000_misaligned": dict(dtype=torch.bfloat16, T=9, H=1000, affine=True, misalign=1),
     "bf16_h16384_T2": dict(dtype=torch.bfloat16, T=2, H=16384, affine=True),
+    # one warp per row (<= 256 vectors, many rows): 1, 4, 5 and 8 vectors per
+    # lane; several warps per row for few rows or longer rows
+    "bf16_h256_T1000": dict(dtype=torch.bfloat16, T=1000, H=256, affine=True),
+    "f16_h1024_T800": dict(dtype=torch.float16, T=800, H=1024, affine=True),
+    "siglip_bf16_h1152_T1000": dict(dtype=torch.bfloat16, T=1000, H=1152, affine=True),
+    "bf16_h2048_T1600_noaffine": dict(dtype=torch.bfloat16, T=1600, H=2048, affine=False),
+    "f16_h640_T33": dict(dtype=torch.float16, T=33, H=640, affine=True),
+    "bf16_h4096_T300": dict(dtype=torch.bfloat16, T=300, H=4096, affine=True),
 }
 
 
@@ -654,7 +662,8 @@ def test_layernorm(name):
     run_ln(LN_CASES[name])
 
 
-@pytest.mark.parametrize("name", ["siglip_bf16_h1152_T512", "f16_h37_generic"])
+@pytest.mark.parametrize("name", ["siglip_bf16_h1152_T512", "f16_h37_generic", "f16_h1024_T800",
+                                  "siglip_bf16_h1152_T1000", "bf16_h4096_T300"])
 def test_layernorm_fp8_and_in_place(name):
     run_ln(LN_CASES[name], fp8=True)
     run_ln(LN_CASES[name], inplace=True)

@@ -683,6 +683,45 @@ def t1_latency(torch, ops, synth, device):
     gu = synth.glu_inputs(0, bf, 1, INTER)["gate_up"].to(device)
     og = torch.empty(1, INTER, dtype=bf, device=device)
     res["glu_silu_d9728"] = measure(lambda: ops.glu_act(gu, ops.SILU, out=og))
+
+    # host cost of one eager call at T = 1 (no graph): validation, dispatch
+    # and cudaLaunchKernelEx in the C library, called once through ctypes
+    # directly and once through the Python binding, on a stream drained every
+    # 64 calls so that the launch queue never fills
+    lib = ops.lib()
+    i = synth.qk_inputs(0, bf, 1, 16, 2, 256, 64, theta=1e7, cache_len=32768,
+                        positions="offset", w_std=0.05)
+    d = {k: v.to(device) for k, v in i.items()}
+    qo, ko = torch.empty_like(d["q"]), torch.empty_like(d["k"])
+    sptr = stream.cuda_stream
+    cargs = (qo.data_ptr(), ko.data_ptr(), ops.BF16, d["q"].data_ptr(), d["k"].data_ptr(),
+             d["wq"].data_ptr(), d["wk"].data_ptr(), ops.BF16, 1, 16, 2, 256, 64,
+             ops.ROTATE_HALF, d["positions"].data_ptr(), d["cos"].data_ptr(),
+             d["sin"].data_ptr(), 32768, EPS, 1, 1.0, sptr)
+
+    def host_us(call, n=2048):
+        for _ in range(64):
+            call()
+        torch.cuda.synchronize()
+        t = 0.0
+        for _ in range(n // 64):
+            t0 = time.perf_counter()
+            for _ in range(64):
+                call()
+            t += time.perf_counter() - t0
+            torch.cuda.synchronize()
+        return round(t / n * 1e6, 3)
+    with torch.cuda.stream(stream):
+        st = lib.edge_qk_norm_rope(*cargs)
+        if st != 0:
+            raise RuntimeError(f"edge_qk_norm_rope returned {ops.STATUS.get(st, st)}")
+        res["host_us_per_eager_call"] = {
+            "qk_norm_rope_16x2_ctypes": host_us(lambda: lib.edge_qk_norm_rope(*cargs)),
+            "qk_norm_rope_16x2_python": host_us(
+                lambda: ops.qk_norm_rope(d["q"], d["k"], d["wq"], d["wk"], d["positions"],
+                                         d["cos"], d["sin"], rotary_dim=64, weight_offset=1,
+                                         q_out=qo, k_out=ko)),
+        }
     return res
 
 

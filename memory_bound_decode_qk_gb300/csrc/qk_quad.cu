@@ -148,10 +148,14 @@ struct QuadHead {
 // PIPE: a resident grid in which every thread issues its next head's loads
 // before the arithmetic of the current one, so that memory and arithmetic
 // overlap across iterations instead of alternating in lockstep waves.
-template <typename T, bool FP8, int C, int LAYOUT, int RQ, bool PIPE, class Map>
+// UNR: the unrounded form (the rotation takes the fp32 normalized value; one
+// rounding after it), for the instantiated geometries only.
+template <typename T, bool FP8, int C, int LAYOUT, int RQ, bool PIPE, class Map, bool UNR = false>
 __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
     constexpr int N = vec_elems<T>();
     constexpr int D = C * K * N;
+    // chunks whose fp32 normalized values the unrounded rotation needs
+    constexpr int RC = UNR ? (LAYOUT == kInterleaved ? RQ : 2 * RQ) : 0;
     static_assert(LAYOUT == kInterleaved ? RQ <= C : 2 * RQ <= C, "rotated chunks exceed the head");
     // w + delta in fp32 (1 when no weight) for q heads, k heads, and 1 for v
     __shared__ __align__(16) float wsm[3][D];
@@ -227,6 +231,7 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
         // q/k rows hold 1.)
         const float* w = wsm[Map::kHasV ? (norm ? un.kind : kKindV) : un.kind];
         uint4 (&mp)[C] = raw;
+        float mf[RC > 0 ? RC : 1][N];  // fp32 normalized values (unrounded form)
 #pragma unroll
         for (int i = 0; i < C; ++i) {
             float x[N], m[N];
@@ -240,8 +245,24 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
                 m[4 * v + 2] = __fmul_rn(__fmul_rn(x[4 * v + 2], r), ww.z);
                 m[4 * v + 3] = __fmul_rn(__fmul_rn(x[4 * v + 3], r), ww.w);
             }
+            if constexpr (RC > 0) {
+                if (i < RC) {
+#pragma unroll
+                    for (int e = 0; e < N; ++e) mf[i < RC ? i : 0][e] = m[e];
+                }
+            }
             mp[i] = pack_vec<T, N>(m);
         }
+        // the value a rotated chunk consumes: the dtype-rounded normalized
+        // value, or its fp32 form in the unrounded mode
+        auto rot_in = [&](int i, float (&a)[N]) {
+            if constexpr (RC > 0) {
+#pragma unroll
+                for (int e = 0; e < N; ++e) a[e] = mf[i < RC ? i : 0][e];
+            } else {
+                unpack_vec<T, N>(mp[i], a);
+            }
+        };
 
         const bool rot = RQ > 0 && pos >= 0 && pos < p.cache_len;
         if (!active || (Map::kHasV && un.dst == nullptr)) return;
@@ -270,7 +291,7 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
                 if (i < RQ && rot) {
                     const int c = kt + K * i;
                     float m[N], y[N], cs[N / 2], sn[N / 2];
-                    unpack_vec<T, N>(mp[i], m);
+                    rot_in(i, m);
                     const float* crow = p.cs + pos * p.half + c * (N / 2);
                     const float* srow = p.sn + pos * p.half + c * (N / 2);
                     if constexpr (N == 8) {
@@ -303,8 +324,8 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
                     // four channels at a time to keep few values live
                     const int c = kt + K * i;
                     float a[N], b[N];
-                    unpack_vec<T, N>(mp[i], a);
-                    unpack_vec<T, N>(mp[i + RQ], b);
+                    rot_in(i, a);
+                    rot_in(i + RQ, b);
                     const float4* c4 = reinterpret_cast<const float4*>(p.cs + pos * p.half + c * N);
                     const float4* s4 = reinterpret_cast<const float4*>(p.sn + pos * p.half + c * N);
 #pragma unroll
@@ -366,11 +387,11 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
     }
 }
 
-template <typename T, bool FP8, int C, int LAYOUT, int RQ>
+template <typename T, bool FP8, int C, int LAYOUT, int RQ, bool UNR = false>
 __global__ void __launch_bounds__(256, (quad_min_blocks<T, FP8, C, LAYOUT, RQ,
                                                         quad_pipe<T, C, LAYOUT, RQ>()>()))
     qk_quad_kernel(QKP p) {
-    quad_body<T, FP8, C, LAYOUT, RQ, quad_pipe<T, C, LAYOUT, RQ>()>(p, QKMap{});
+    quad_body<T, FP8, C, LAYOUT, RQ, quad_pipe<T, C, LAYOUT, RQ>(), QKMap, UNR>(p, QKMap{});
 }
 
 template <typename T, int C, int LAYOUT, int RQ>
@@ -466,7 +487,7 @@ template <typename T, bool FP8>
 cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg, bool* handled) {
     constexpr int N = vec_elems<T>();
     *handled = false;
-    if (a.mode & kModeUnrounded) return cudaSuccess;  // served by the lane-group path
+    const bool unr = (a.mode & kModeUnrounded) != 0;
     // FP8 outputs are N bytes per chunk: alignment N
     if ((a.q_out && reinterpret_cast<uintptr_t>(a.q_out) % (FP8 ? N : 16) != 0) ||
         (a.k_out && reinterpret_cast<uintptr_t>(a.k_out) % (FP8 ? N : 16) != 0)) {
@@ -478,10 +499,24 @@ cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg
         return cudaSuccess;
     }
     void (*fn)(QKP) = nullptr;
-    switch (C) {
-        case 2: fn = pick_rq<QKSel, T, FP8, 2>(a.layout, rq); break;
-        case 4: fn = pick_rq<QKSel, T, FP8, 4>(a.layout, rq); break;
-        default: fn = pick_rq<QKSel, T, FP8, 8>(a.layout, rq); break;
+    if (unr) {
+        // the unrounded form for 16-bit rotate-half heads of 512 bytes with
+        // rotary 64 (the text profiles) and of 256 bytes rotating fully;
+        // other geometries take the lane-group path
+        if constexpr (sizeof(T) == 2) {
+            if (a.layout == kRotateHalf && C == 8 && rq == 1) {
+                fn = qk_quad_kernel<T, FP8, 8, kRotateHalf, 1, true>;
+            }
+            if (a.layout == kRotateHalf && C == 4 && rq == 2) {
+                fn = qk_quad_kernel<T, FP8, 4, kRotateHalf, 2, true>;
+            }
+        }
+    } else {
+        switch (C) {
+            case 2: fn = pick_rq<QKSel, T, FP8, 2>(a.layout, rq); break;
+            case 4: fn = pick_rq<QKSel, T, FP8, 4>(a.layout, rq); break;
+            default: fn = pick_rq<QKSel, T, FP8, 8>(a.layout, rq); break;
+        }
     }
     if (fn == nullptr) return cudaSuccess;
     *handled = true;

@@ -588,24 +588,38 @@ def test_rope_fp8(name):
 
 # ---------------------------------------------------------------- review variant
 
+@pytest.mark.parametrize("fp8", [False, True])
 @pytest.mark.parametrize("name", ["cfg3_16_2_T333", "cfg4_bf16", "cfg1_f32", "generic_rot24",
-                                  "quad_cfg4_interleaved", "d128_bf16", "generic_odd_d37"])
-def test_qk_norm_rope_unrounded(name):
-    # rotation of the fp32 normalized value, one rounding (ninfer review, item 1)
+                                  "quad_cfg4_interleaved", "d128_bf16", "generic_odd_d37",
+                                  "quad_no_weight", "dflash2_W16_B32"])
+def test_qk_norm_rope_unrounded(name, fp8):
+    # rotation of the fp32 normalized value, one rounding (ninfer review,
+    # item 1); quad_no_weight and dflash2_W16_B32 take four threads per head
     c = QK_CASES[name]
     dtype, fmt = c["dtype"], TORCH_FMT[c["dtype"]]
     inp = synth.qk_inputs(0, dtype, c["T"], c["Hq"], c["Hk"], c["D"], c["rot"],
                           theta=c["theta"], cache_len=c["P"], positions=c["positions"],
                           w_mean=c["w_mean"] or 0.0, w_std=c["w_std"])
-    ref = oracle.qk_norm_rope(storage(inp["q"]), storage(inp["k"]), storage(inp["wq"]),
-                              storage(inp["wk"]), fmt, c["rot"], c["layout"],
-                              inp["positions"].numpy(), storage(inp["cos"]), storage(inp["sin"]),
-                              1e-6, c["offset"], eta=ETA_NORM, unrounded=True)
-    d = {n: dev(inp[n]) for n in ("q", "k", "wq", "wk", "positions", "cos", "sin")}
-    qo, ko = edge_ops.qk_norm_rope(d["q"], d["k"], d["wq"], d["wk"], d["positions"], d["cos"],
+    wq = None if inp["wq"] is None or c["w_mean"] is None else storage(inp["wq"])
+    wk = None if inp["wk"] is None or c["w_mean"] is None else storage(inp["wk"])
+    inv = 40.0 if fp8 else 1.0
+    ref = oracle.qk_norm_rope(storage(inp["q"]), storage(inp["k"]), wq, wk, fmt, c["rot"],
+                              c["layout"], inp["positions"].numpy(), storage(inp["cos"]),
+                              storage(inp["sin"]), 1e-6, c["offset"],
+                              out_fmt=oracle.E4M3 if fp8 else fmt, inv_scale=inv, eta=ETA_NORM,
+                              unrounded=True)
+    d = {n: dev(inp[n]) for n in ("q", "k", "positions", "cos", "sin")}
+    dwq = None if wq is None else dev(inp["wq"])
+    dwk = None if wk is None else dev(inp["wk"])
+    qo, ko = edge_ops.qk_norm_rope(d["q"], d["k"], dwq, dwk, d["positions"], d["cos"],
                                    d["sin"], rotary_dim=c["rot"], layout=c["layout"], eps=1e-6,
-                                   weight_offset=c["offset"], cache_len=c["P"], unrounded=True)
+                                   weight_offset=c["offset"], cache_len=c["P"], unrounded=True,
+                                   fp8=fp8, inv_scale=inv)
     torch.cuda.synchronize()
+    if fp8:
+        check_fp8_out(name + " q", qo.cpu().numpy(), ref.q_lo, ref.q_hi, ref.q_mag, ETA_NORM, inv)
+        check_fp8_out(name + " k", ko.cpu().numpy(), ref.k_lo, ref.k_hi, ref.k_mag, ETA_NORM, inv)
+        return
     check_out(name + " q", storage(qo.cpu()), ref.q_out, ref.q_pre, ref.q_mag, fmt, fmt,
               ETA_NORM, lo=ref.q_lo, hi=ref.q_hi)
     check_out(name + " k", storage(ko.cpu()), ref.k_out, ref.k_pre, ref.k_mag, fmt, fmt,

@@ -91,8 +91,15 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+# The current stream's raw handle without building a Stream object (about 2
+# us cheaper per call); the public route where torch lacks it.
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
     if stream is None:
+        if _RAW_STREAM is not None:
+            return _RAW_STREAM(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
 

@@ -180,24 +180,11 @@ __global__ void __launch_bounds__(256) rows_generic_kernel(RowsP p) {
     }
 }
 
-// Sum of v over the W warps that own a row (one shuffle tree per warp, then
-// shared memory).  Every thread of the CTA calls it the same number of times.
-__device__ __forceinline__ float row_sum(float v, const RowsP& p, int g, int lane, int wib,
-                                         float* red) {
-    v = group_sum<32>(v);
-    if (p.W > 1) {
-        if (lane == 0) red[wib] = v;
-        __syncthreads();
-        v = 0.0f;
-        for (int k = 0; k < p.W; ++k) v = __fadd_rn(v, red[g * p.W + k]);
-        __syncthreads();
-    }
-    return v;
-}
-
-// row_sum with one barrier: the partial sums go to `buf`, which the caller
-// alternates between two reductions, so a buffer is rewritten only after a
-// later barrier that every reader of its previous contents has passed.
+// Sum of v over the W warps that own a row: one shuffle tree per warp, then
+// shared memory, with one barrier.  Every thread of the CTA calls it the same
+// number of times.  The partial sums go to `buf`, which the caller alternates
+// between two reductions, so a buffer is rewritten only after a later barrier
+// that every reader of its previous contents has passed.
 __device__ __forceinline__ float row_sum_alt(float v, const RowsP& p, int g, int lane, int wib,
                                              float* buf) {
     v = group_sum<32>(v);

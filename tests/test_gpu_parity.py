@@ -804,3 +804,53 @@ def run_qkv(c):
 @pytest.mark.parametrize("name", list(QKV_CASES))
 def test_qkv_rope_cache(name):
     run_qkv(QKV_CASES[name])
+
+
+# ---------------------------------------------------------------- the benchmark's step
+
+def test_benchmark_decode_step_matches_oracle():
+    # The benchmark's own step: 36 layers of seam ops on its per-layer buffers,
+    # replayed once from its captured CUDA graph (the launch configuration the
+    # benchmark times).  Capturing runs the step once eagerly, so layers 0 and
+    # 35 are checked against the oracle applied to their state just before
+    # the replay.
+    import bench
+
+    layers, sh = bench.build_layers(torch, synth, torch.device("cuda"), seed=0)
+    stream = torch.cuda.Stream()
+
+    def step():
+        for L in layers:
+            for _, fn in bench.layer_ops(edge_ops, L, sh):
+                fn()
+    graph = bench.capture(torch, step, stream)
+    names = ("res", "q", "k", "mlp_out", "attn_out", "gate_up")
+    checked = (0, len(layers) - 1)
+    before = {i: {n: storage(getattr(layers[i], n).cpu()) for n in names} for i in checked}
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    fmt = oracle.BF16
+    pos, cos, sin = (sh[n].cpu().numpy() for n in ("pos", "cos", "sin"))
+    for i in checked:
+        L, b = layers[i], before[i]
+        h1, res1, pre1 = oracle.add_rmsnorm(b["mlp_out"], b["res"], storage(L.w_in.cpu()), fmt,
+                                            bench.EPS)
+        qk = oracle.qk_norm_rope(b["q"], b["k"], storage(L.wq.cpu()), storage(L.wk.cpu()), fmt,
+                                 bench.HD, oracle.ROTATE_HALF, pos, cos, sin, bench.EPS, 0,
+                                 eta=ETA_NORM)
+        h2, res2, pre2 = oracle.add_rmsnorm(b["attn_out"], res1, storage(L.w_post.cpu()), fmt,
+                                            bench.EPS)
+        act, prea = oracle.glu_act(b["gate_up"], fmt, oracle.SILU)
+        assert np.array_equal(storage(L.res.cpu()), res2), f"layer {i}: residual not bit-exact"
+        check_out(f"layer {i} h1", storage(L.h1.cpu()), h1, pre1, np.abs(pre1), fmt, fmt,
+                  ETA_NORM)
+        check_out(f"layer {i} h2", storage(L.h2.cpu()), h2, pre2, np.abs(pre2), fmt, fmt,
+                  ETA_NORM)
+        check_out(f"layer {i} q", storage(L.q.cpu()), qk.q_out, qk.q_pre, qk.q_mag, fmt, fmt,
+                  ETA_NORM, lo=qk.q_lo, hi=qk.q_hi)
+        check_out(f"layer {i} k", storage(L.k.cpu()), qk.k_out, qk.k_pre, qk.k_mag, fmt, fmt,
+                  ETA_NORM, lo=qk.k_lo, hi=qk.k_hi)
+        gate = oracle.decode(b["gate_up"], fmt)[:, :bench.INTER]
+        check_out(f"layer {i} act", storage(L.act.cpu()), act, prea, np.abs(prea), fmt, fmt,
+                  gate_eta(gate, oracle.SILU))

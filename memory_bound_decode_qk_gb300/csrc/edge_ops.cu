@@ -89,6 +89,11 @@ int rows_vt_override() {
     return v;
 }
 
+int quad_threads_override() {
+    static const int v = env_choice("EDGE_OPS_QUAD_THREADS", {64, 128, 256});
+    return v;
+}
+
 int ln_warp_override() {
     static const int v = [] {
         const char* e = std::getenv("EDGE_OPS_LN_WARP");

@@ -327,6 +327,10 @@ cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg
 // lane-group path's grid exceeds one wave of resident CTAs.
 bool quad_suits(int layout, int rotary_dim, int64_t head_bytes);
 
+// Waves of the lane-group grid beyond which the four-threads-per-head path
+// takes over the prologue (measured per geometry).
+double quad_min_waves(int elem_bytes, int layout, int rotary_dim, int64_t head_bytes);
+
 // Arguments of the fused QKV kernels: the prologue's QKP (q = the fused qkv
 // rows, qo = q_out; k and ko unused) and the cache side.
 struct QKVP {

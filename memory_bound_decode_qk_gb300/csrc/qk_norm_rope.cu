@@ -148,13 +148,13 @@ cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
         int path = qk_path_override();
         if (path == 0) {
             // Measured on GB300 for every geometry: the one-shot grid wins
-            // while it fits in one wave of resident CTAs; past that, four
-            // threads per head (about 4x fewer instructions per head) win.
-            const int64_t wave = (int64_t)resident_ctas((const void*)vfn, threads) * sms;
-            path = blocks > wave &&
-                           quad_suits(a.layout, a.rotary_dim, (int64_t)D * (int64_t)sizeof(T))
-                       ? 3
-                       : 1;
+            // up to a geometry's fraction of one wave of resident CTAs;
+            // past that, four threads per head (about 4x fewer instructions
+            // per head) win.
+            const int64_t hbytes = (int64_t)D * (int64_t)sizeof(T);
+            const double wave = (double)resident_ctas((const void*)vfn, threads) * sms *
+                                quad_min_waves((int)sizeof(T), a.layout, a.rotary_dim, hbytes);
+            path = (double)blocks > wave && quad_suits(a.layout, a.rotary_dim, hbytes) ? 3 : 1;
         }
         if (path == 3) {
             bool handled = false;

@@ -467,9 +467,15 @@ bool pipe_of(int C, int layout, int rq) {
     return C == 8 && !(sizeof(T) == 2 && (layout == kInterleaved || 2 * rq > 2));
 }
 
+// Threads per CTA: small CTAs spread mid-size work over every SM (16 heads
+// per CTA for 512-byte heads, 32 for smaller ones).  Measured on GB300 at
+// T = 128 to 4096: up to 25% faster than 64 heads per CTA at mid T, within
+// a few percent at large T.
 template <typename P, typename Fn>
-cudaError_t launch_quad(Fn fn, const P& arg, uint32_t units, bool pipe, cudaLaunchConfig_t cfg) {
-    const int threads = 256;
+cudaError_t launch_quad(Fn fn, const P& arg, uint32_t units, bool pipe, int C,
+                        cudaLaunchConfig_t cfg) {
+    int threads = C == 8 ? 64 : 128;
+    if (quad_threads_override() > 0) threads = quad_threads_override();
     const int64_t per_block = threads / K;
     int64_t blocks = ((int64_t)units + per_block - 1) / per_block;
     // the load-ahead form needs every CTA resident for all its passes
@@ -520,7 +526,7 @@ cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg
     }
     if (fn == nullptr) return cudaSuccess;
     *handled = true;
-    return launch_quad(fn, p, p.units, pipe_of<T>(C, a.layout, rq), cfg);
+    return launch_quad(fn, p, p.units, pipe_of<T>(C, a.layout, rq), C, cfg);
 }
 
 template <typename T>
@@ -540,7 +546,20 @@ cudaError_t launch_qkv_quad(const QKVArgs& a, const QKVP& k, cudaLaunchConfig_t 
     }
     if (fn == nullptr) return cudaSuccess;
     *handled = true;
-    return launch_quad(fn, k, k.p.units, pipe_of<T>(C, a.layout, rq), cfg);
+    return launch_quad(fn, k, k.p.units, pipe_of<T>(C, a.layout, rq), C, cfg);
+}
+
+double quad_min_waves(int elem_bytes, int layout, int rotary_dim, int64_t head_bytes) {
+    // Measured on GB300 (lane-group against four threads per head, T = 1 to
+    // 4096, with 16- or 32-head CTAs): 16-bit 256- and 512-byte heads with at
+    // most two rotate-half chunks per thread cross at about half a wave of
+    // the lane-group grid (text profiles, FP8 out, DFlash2, context-K);
+    // 16-bit 512-byte heads rotating fully at one wave; fp32 heads at about
+    // one and a half.  Unmeasured geometries keep one wave.
+    if (elem_bytes == 4) return 1.5;
+    const bool heavy = head_bytes == 512 && (layout == kInterleaved || rotary_dim > 64);
+    if ((head_bytes == 256 || head_bytes == 512) && !heavy) return 0.5;
+    return 1.0;
 }
 
 bool quad_suits(int layout, int rotary_dim, int64_t head_bytes) {

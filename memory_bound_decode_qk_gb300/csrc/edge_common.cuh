@@ -150,9 +150,10 @@ __device__ __forceinline__ uint8_t quantize1(float y, float inv) {
 
 // ---------------------------------------------------------------- reductions
 
-// Sum over aligned groups of G lanes (G a power of two <= 32).
-template <int G>
-__device__ __forceinline__ float group_sum(float v) {
+// Sum over aligned groups of G lanes (G a power of two <= 32), of float or
+// double values.
+template <int G, typename V>
+__device__ __forceinline__ V group_sum(V v) {
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;

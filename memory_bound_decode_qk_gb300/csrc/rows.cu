@@ -83,7 +83,9 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
             wr[i] = (ok && wv != nullptr) ? __ldg(wv + idx) : make_uint4(0u, 0u, 0u, 0u);
         }
 
-        float ss = 0.0f;
+        // two running sums, alternating by vector: at most 4N sequential
+        // terms each, for the error bound of the tolerance
+        float ssp[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             float a[N];
@@ -99,9 +101,9 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
                 if (active && idx < p.nvec) rr[idx] = xv[i];
             }
 #pragma unroll
-            for (int e = 0; e < N; ++e) ss = __fmaf_rn(a[e], a[e], ss);
+            for (int e = 0; e < N; ++e) ssp[i & 1] = __fmaf_rn(a[e], a[e], ssp[i & 1]);
         }
-        ss = group_sum<32>(ss);
+        float ss = group_sum<32>(__fadd_rn(ssp[0], ssp[1]));
         if (p.W > 1) {
             if (lane == 0) red[wib] = ss;
             __syncthreads();
@@ -138,8 +140,11 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
 }
 
 template <typename T, bool FP8, bool ADD>
+// The row's sum of squares is accumulated in fp64: a thread here sums
+// hidden / 256 terms (65,536 at the largest row), too many for an fp32
+// running sum to stay within a few fp32 ulps.
 __global__ void __launch_bounds__(256) rows_generic_kernel(RowsP p) {
-    __shared__ float red[8];
+    __shared__ double red[8];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int nw = blockDim.x >> 5;
@@ -150,22 +155,22 @@ __global__ void __launch_bounds__(256) rows_generic_kernel(RowsP p) {
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
         const T* x = reinterpret_cast<const T*>(p.x) + row * p.hidden;
         T* res = ADD ? reinterpret_cast<T*>(p.res) + row * p.hidden : nullptr;
-        float ss = 0.0f;
+        double ss = 0.0;
         for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
             float a = to_f(x[i]);
             if constexpr (ADD) {
                 a = round_to<T>(__fadd_rn(a, to_f(res[i])));
                 res[i] = from_f<T>(a);
             }
-            ss = __fmaf_rn(a, a, ss);
+            ss = __fma_rn((double)a, (double)a, ss);
         }
         ss = group_sum<32>(ss);
         if (lane == 0) red[wib] = ss;
         __syncthreads();
-        ss = 0.0f;
-        for (int k = 0; k < nw; ++k) ss = __fadd_rn(ss, red[k]);
+        ss = 0.0;
+        for (int k = 0; k < nw; ++k) ss = __dadd_rn(ss, red[k]);
         __syncthreads();
-        const float r = inv_rms(ss, p.invH, p.eps);
+        const float r = inv_rms((float)ss, p.invH, p.eps);
         const T* w = reinterpret_cast<const T*>(p.w);
         for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
             const float s = ADD ? to_f(res[i]) : to_f(x[i]);
@@ -239,16 +244,17 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
             const bool ok = active && idx < p.nvec;
             xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float sum = 0.0f;
+        float sp[2] = {0.0f, 0.0f};  // two running sums, alternating by vector
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             float a[N];
             unpack_vec<T, N>(xv[i], a);
 #pragma unroll
-            for (int e = 0; e < N; ++e) sum = __fadd_rn(sum, a[e]);
+            for (int e = 0; e < N; ++e) sp[i & 1] = __fadd_rn(sp[i & 1], a[e]);
         }
+        const float sum = __fadd_rn(sp[0], sp[1]);
         const float mu = __fmul_rn(row_sum_alt(sum, p, g, lane, wib, red_mu), p.invH);
-        float sq = 0.0f;
+        float sqp[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int idx = tid + i * tpr;
@@ -258,9 +264,10 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
 #pragma unroll
             for (int e = 0; e < N; ++e) {
                 const float d = __fsub_rn(a[e], mu);
-                sq = __fmaf_rn(d, d, sq);
+                sqp[i & 1] = __fmaf_rn(d, d, sqp[i & 1]);
             }
         }
+        const float sq = __fadd_rn(sqp[0], sqp[1]);
         const float r = inv_rms(row_sum_alt(sq, p, g, lane, wib, red_var), p.invH, p.eps);
         // gamma and beta (L1/L2-resident), all issued before the output loop
         uint4 gr[V], br[V];
@@ -361,16 +368,17 @@ __global__ void __launch_bounds__(256, ln_warp_min_blocks<V>()) ln_warp_kernel(R
             __syncthreads();
             staged = true;
         }
-        float sum = 0.0f;
+        float sp[2] = {0.0f, 0.0f};  // two running sums, alternating by vector
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             float a[N];
             unpack_vec<T, N>(xv[i], a);
 #pragma unroll
-            for (int e = 0; e < N; ++e) sum = __fadd_rn(sum, a[e]);
+            for (int e = 0; e < N; ++e) sp[i & 1] = __fadd_rn(sp[i & 1], a[e]);
         }
+        const float sum = __fadd_rn(sp[0], sp[1]);
         const float mu = __fmul_rn(group_sum<32>(sum), p.invH);
-        float sq = 0.0f;
+        float sqp[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             if (lane + 32 * i >= p.nvec) continue;  // padding lanes add nothing
@@ -379,9 +387,10 @@ __global__ void __launch_bounds__(256, ln_warp_min_blocks<V>()) ln_warp_kernel(R
 #pragma unroll
             for (int e = 0; e < N; ++e) {
                 const float d = __fsub_rn(a[e], mu);
-                sq = __fmaf_rn(d, d, sq);
+                sqp[i & 1] = __fmaf_rn(d, d, sqp[i & 1]);
             }
         }
+        const float sq = __fadd_rn(sqp[0], sqp[1]);
         const float r = inv_rms(group_sum<32>(sq), p.invH, p.eps);
         if (!active) continue;
         char* orow = p.out + row * out_row;
@@ -413,17 +422,18 @@ __global__ void __launch_bounds__(256, ln_warp_min_blocks<V>()) ln_warp_kernel(R
 // Any size or alignment: one CTA per row, three passes (the second and third
 // hit L1/L2).
 template <typename T, bool FP8>
+// Both reductions accumulate in fp64, as in the scalar RMSNorm kernel.
 __global__ void __launch_bounds__(256) ln_generic_kernel(RowsP p) {
-    __shared__ float red[8];
+    __shared__ double red[8];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int nw = blockDim.x >> 5;
-    auto block_sum = [&](float v) {
+    auto block_sum = [&](double v) {
         v = group_sum<32>(v);
         if (lane == 0) red[wib] = v;
         __syncthreads();
-        v = 0.0f;
-        for (int k = 0; k < nw; ++k) v = __fadd_rn(v, red[k]);
+        v = 0.0;
+        for (int k = 0; k < nw; ++k) v = __dadd_rn(v, red[k]);
         __syncthreads();
         return v;
     };
@@ -435,15 +445,17 @@ __global__ void __launch_bounds__(256) ln_generic_kernel(RowsP p) {
     const T* bt = reinterpret_cast<const T*>(p.beta);
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
         const T* x = reinterpret_cast<const T*>(p.x) + row * p.hidden;
-        float sum = 0.0f;
-        for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) sum = __fadd_rn(sum, to_f(x[i]));
-        const float mu = __fmul_rn(block_sum(sum), p.invH);
-        float sq = 0.0f;
+        double sum = 0.0;
+        for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
+            sum = __dadd_rn(sum, (double)to_f(x[i]));
+        }
+        const float mu = (float)(block_sum(sum) / (double)p.hidden);
+        double sq = 0.0;
         for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
             const float d = __fsub_rn(to_f(x[i]), mu);
-            sq = __fmaf_rn(d, d, sq);
+            sq = __fma_rn((double)d, (double)d, sq);
         }
-        const float r = inv_rms(block_sum(sq), p.invH, p.eps);
+        const float r = inv_rms((float)block_sum(sq), p.invH, p.eps);
         for (int i = threadIdx.x; i < p.hidden; i += blockDim.x) {
             float v = __fmul_rn(__fsub_rn(to_f(x[i]), mu), r);
             if (gm != nullptr) v = __fmul_rn(v, to_f(gm[i]));

@@ -159,6 +159,18 @@ def test_zero_rows_is_ok_and_launches_nothing(L):
     (lambda L: L.edge_qkv_rope_cache(QO, KO, KO + 65536, Q, WQ, WK, FP8, 4, 8, 2, 128, 64, 0,
                                      POS, COS, SIN, 4096, POS + 4096, 16, 1e-6, 0, 1, None), DTYPE),
     (lambda L: rms(L, hidden=2 ** 25, rows=1), UNSUP),
+    # one past each declared limit: rows of 2**24, heads of 2048, 2**31 - 1 units
+    (lambda L: rms(L, hidden=2 ** 24 + 8, rows=1), UNSUP),
+    (lambda L: add(L, hidden=2 ** 24 + 8, rows=1), UNSUP),
+    (lambda L: L.edge_layernorm(O, BF16, X, W, None, BF16, 1, 2 ** 24 + 8, 1e-5, 1.0, None),
+     UNSUP),
+    (lambda L: qk(L, D=2050, rot=64), UNSUP),
+    (lambda L: qk(L, T=2 ** 28, Hq=8, Hk=0, k=None), UNSUP),
+    (lambda L: L.edge_rope(QO, KO, BF16, Q, K, BF16, 4, 8, 2, 2050, 64, 0, POS, COS, SIN,
+                           4096, 1.0, None), UNSUP),
+    (lambda L: L.edge_qkv_rope_cache(QO, KO, KO + 2 ** 20, Q, WQ, WK, BF16, 4, 8, 2, 2050, 64, 0,
+                                     POS, COS, SIN, 4096, POS + 4096, 16, 1e-6, 0, 1, None),
+     UNSUP),
 ])
 def test_invalid_calls_are_rejected(L, call, status):
     assert call(L) == status

@@ -854,3 +854,37 @@ def test_benchmark_decode_step_matches_oracle():
         gate = oracle.decode(b["gate_up"], fmt)[:, :bench.INTER]
         check_out(f"layer {i} act", storage(L.act.cpu()), act, prea, np.abs(prea), fmt, fmt,
                   gate_eta(gate, oracle.SILU))
+
+
+# ---------------------------------------------------------------- the declared size limits
+
+def test_rows_at_the_largest_row():
+    # hidden = 2**24, the largest row the library takes (the scalar path, one
+    # CTA per row, fp64 reductions)
+    c = dict(dtype=torch.bfloat16, T=1, H=1 << 24, w_mean=1.0, w_std=0.02, off=0)
+    run_rows(c, fused=True)
+    run_rows(dict(c, w_mean=0.0, off=1), fused=False)
+
+
+def test_layernorm_at_the_largest_row():
+    run_ln(dict(dtype=torch.bfloat16, T=1, H=1 << 24, affine=True))
+
+
+@pytest.mark.parametrize("c", [
+    dict(dtype=torch.bfloat16, T=3, Hq=2, Hk=1, D=2048, rot=2048, layout=0, w_mean=0.0,
+         w_std=0.1, offset=1, theta=1e4, P=16, positions="arange"),
+    dict(dtype=torch.float16, T=2, Hq=1, Hk=2, D=2048, rot=1024, layout=1, w_mean=1.0,
+         w_std=0.02, offset=0, theta=1e4, P=8, positions=np.array([3, 9])),
+])
+def test_qk_at_the_largest_head(c):
+    # head_dim = 2048, the largest head the prologue takes
+    ref, gq, gk, fmt, out_fmt, _ = run_qk(c)
+    check_out("q", gq, ref.q_out, ref.q_pre, ref.q_mag, fmt, out_fmt, ETA_NORM, lo=ref.q_lo,
+              hi=ref.q_hi)
+    check_out("k", gk, ref.k_out, ref.k_pre, ref.k_mag, fmt, out_fmt, ETA_NORM, lo=ref.k_lo,
+              hi=ref.k_hi)
+
+
+def test_qkv_at_the_largest_head():
+    run_qkv(dict(dtype=torch.bfloat16, T=3, Hq=2, Hk=1, D=2048, rot=1024, layout=0, norm=True,
+                 offset=1, S=4))

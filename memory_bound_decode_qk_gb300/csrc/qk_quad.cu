@@ -210,17 +210,21 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
         const QuadUnit& un = h.un;
         const bool active = h.active, isv = h.isv;
         const int64_t pos = h.pos;
-        // two running sums, alternating by chunk: at most 4N sequential terms
-        // each, for the error bound of the tolerance
+        // beyond 32 terms per thread, two running sums alternating by chunk
+        // (at most 4N sequential terms each, for the error bound of the
+        // tolerance)
+        constexpr bool kSplit = C * N > 32;
         float ssp[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < C; ++i) {
             float x[N];
             unpack_vec<T, N>(raw[i], x);
 #pragma unroll
-            for (int e = 0; e < N; ++e) ssp[i & 1] = __fmaf_rn(x[e], x[e], ssp[i & 1]);
+            for (int e = 0; e < N; ++e) {
+                ssp[kSplit ? (i & 1) : 0] = __fmaf_rn(x[e], x[e], ssp[kSplit ? (i & 1) : 0]);
+            }
         }
-        float ss = __fadd_rn(ssp[0], ssp[1]);
+        float ss = kSplit ? __fadd_rn(ssp[0], ssp[1]) : ssp[0];
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         ss += __shfl_xor_sync(0xffffffffu, ss, 2);
         // without normalization (standalone rotary, the unnormalized QKV

@@ -83,8 +83,10 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
             wr[i] = (ok && wv != nullptr) ? __ldg(wv + idx) : make_uint4(0u, 0u, 0u, 0u);
         }
 
-        // two running sums, alternating by vector: at most 4N sequential
-        // terms each, for the error bound of the tolerance
+        // beyond 32 terms per thread, two running sums alternating by vector
+        // (at most 4N sequential terms each, for the error bound of the
+        // tolerance)
+        constexpr bool kSplit = V * N > 32;
         float ssp[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < V; ++i) {
@@ -101,9 +103,11 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
                 if (active && idx < p.nvec) rr[idx] = xv[i];
             }
 #pragma unroll
-            for (int e = 0; e < N; ++e) ssp[i & 1] = __fmaf_rn(a[e], a[e], ssp[i & 1]);
+            for (int e = 0; e < N; ++e) {
+                ssp[kSplit ? (i & 1) : 0] = __fmaf_rn(a[e], a[e], ssp[kSplit ? (i & 1) : 0]);
+            }
         }
-        float ss = group_sum<32>(__fadd_rn(ssp[0], ssp[1]));
+        float ss = group_sum<32>(kSplit ? __fadd_rn(ssp[0], ssp[1]) : ssp[0]);
         if (p.W > 1) {
             if (lane == 0) red[wib] = ss;
             __syncthreads();
@@ -244,15 +248,19 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
             const bool ok = active && idx < p.nvec;
             xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float sp[2] = {0.0f, 0.0f};  // two running sums, alternating by vector
+        // beyond 32 terms per thread, two running sums alternating by vector
+        constexpr bool kSplit = V * N > 32;
+        float sp[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             float a[N];
             unpack_vec<T, N>(xv[i], a);
 #pragma unroll
-            for (int e = 0; e < N; ++e) sp[i & 1] = __fadd_rn(sp[i & 1], a[e]);
+            for (int e = 0; e < N; ++e) {
+                sp[kSplit ? (i & 1) : 0] = __fadd_rn(sp[kSplit ? (i & 1) : 0], a[e]);
+            }
         }
-        const float sum = __fadd_rn(sp[0], sp[1]);
+        const float sum = kSplit ? __fadd_rn(sp[0], sp[1]) : sp[0];
         const float mu = __fmul_rn(row_sum_alt(sum, p, g, lane, wib, red_mu), p.invH);
         float sqp[2] = {0.0f, 0.0f};
 #pragma unroll
@@ -264,10 +272,10 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
 #pragma unroll
             for (int e = 0; e < N; ++e) {
                 const float d = __fsub_rn(a[e], mu);
-                sqp[i & 1] = __fmaf_rn(d, d, sqp[i & 1]);
+                sqp[kSplit ? (i & 1) : 0] = __fmaf_rn(d, d, sqp[kSplit ? (i & 1) : 0]);
             }
         }
-        const float sq = __fadd_rn(sqp[0], sqp[1]);
+        const float sq = kSplit ? __fadd_rn(sqp[0], sqp[1]) : sqp[0];
         const float r = inv_rms(row_sum_alt(sq, p, g, lane, wib, red_var), p.invH, p.eps);
         // gamma and beta (L1/L2-resident), all issued before the output loop
         uint4 gr[V], br[V];
@@ -368,15 +376,19 @@ __global__ void __launch_bounds__(256, ln_warp_min_blocks<V>()) ln_warp_kernel(R
             __syncthreads();
             staged = true;
         }
-        float sp[2] = {0.0f, 0.0f};  // two running sums, alternating by vector
+        // beyond 32 terms per thread, two running sums alternating by vector
+        constexpr bool kSplit = V * N > 32;
+        float sp[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             float a[N];
             unpack_vec<T, N>(xv[i], a);
 #pragma unroll
-            for (int e = 0; e < N; ++e) sp[i & 1] = __fadd_rn(sp[i & 1], a[e]);
+            for (int e = 0; e < N; ++e) {
+                sp[kSplit ? (i & 1) : 0] = __fadd_rn(sp[kSplit ? (i & 1) : 0], a[e]);
+            }
         }
-        const float sum = __fadd_rn(sp[0], sp[1]);
+        const float sum = kSplit ? __fadd_rn(sp[0], sp[1]) : sp[0];
         const float mu = __fmul_rn(group_sum<32>(sum), p.invH);
         float sqp[2] = {0.0f, 0.0f};
 #pragma unroll
@@ -387,10 +399,10 @@ __global__ void __launch_bounds__(256, ln_warp_min_blocks<V>()) ln_warp_kernel(R
 #pragma unroll
             for (int e = 0; e < N; ++e) {
                 const float d = __fsub_rn(a[e], mu);
-                sqp[i & 1] = __fmaf_rn(d, d, sqp[i & 1]);
+                sqp[kSplit ? (i & 1) : 0] = __fmaf_rn(d, d, sqp[kSplit ? (i & 1) : 0]);
             }
         }
-        const float sq = __fadd_rn(sqp[0], sqp[1]);
+        const float sq = kSplit ? __fadd_rn(sqp[0], sqp[1]) : sqp[0];
         const float r = inv_rms(group_sum<32>(sq), p.invH, p.eps);
         if (!active) continue;
         char* orow = p.out + row * out_row;

@@ -323,8 +323,8 @@ __device__ void generic_head(const QKP& p, const char* src, char* dst, const cha
 template <typename T, bool FP8>
 cudaError_t launch_qk_quad(const QKArgs& a, const QKP& p, cudaLaunchConfig_t cfg, bool* handled);
 
-// Whether the four-threads-per-head path suits a geometry once the
-// lane-group path's grid exceeds one wave of resident CTAs.
+// Whether the four-threads-per-head path suits a geometry at all (past the
+// geometry's quad_min_waves of the lane-group grid).
 bool quad_suits(int layout, int rotary_dim, int64_t head_bytes);
 
 // Waves of the lane-group grid beyond which the four-threads-per-head path

@@ -18,6 +18,8 @@
 //   - cos/sin entries are read from L1: every head of a token shares the row.
 // Units are ordered token-major, so the warps of a CTA share cos/sin rows and
 // the norm weights.  Streamed inputs use evict-first loads.
+// Many heads: the four-threads-per-head path (qk_quad.cu) takes over past a
+// measured fraction of one wave of this path's grid (quad_min_waves).
 // Generic path: one warp per head, staged through shared memory.  It serves
 // any head_dim up to 2048, any even rotary_dim and any element-aligned
 // pointer.

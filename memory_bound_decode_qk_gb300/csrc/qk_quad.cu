@@ -41,10 +41,11 @@ namespace {
 
 constexpr int K = 4;  // threads per head
 
-// CTAs per SM that the register budget is sized for (65536 registers per SM,
-// 256 threads per CTA).  Fewer elements per thread leave fewer live values,
-// so more CTAs fit: 5 (51 registers) for 128-byte heads and 4 (64) for
-// 256-byte heads, both without spills; 3 (85) for 512-byte heads; 2 (128)
+// Register budget per thread, stated as CTAs of 256 threads per SM (65536
+// registers per SM); the 64- and 128-thread CTAs used at launch hold the same
+// registers per thread.  Fewer elements per thread leave fewer live values,
+// so more threads fit: 5 CTAs (51 registers) for 128-byte heads and 4 (64)
+// for 256-byte heads, both without spills; 3 (85) for 512-byte heads; 2 (128)
 // with the FP8 epilogue, and for 16-bit 512-byte heads (64 elements per
 // thread) that are interleaved or have more than two rotate-half chunks per
 // thread.  Measured on GB300: those 16-bit heads ran faster at 2 CTAs than at

@@ -94,6 +94,11 @@ int quad_threads_override() {
     return v;
 }
 
+int ln_warp_threads_override() {
+    static const int v = env_choice("EDGE_OPS_LN_WARP_THREADS", {32, 64, 128, 256});
+    return v;
+}
+
 int ln_warp_override() {
     static const int v = [] {
         const char* e = std::getenv("EDGE_OPS_LN_WARP");

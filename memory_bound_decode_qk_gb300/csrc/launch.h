@@ -112,6 +112,9 @@ int glu_unroll_override();
 // EDGE_OPS_LN_WARP: 1 one warp per LayerNorm row, 0 never; -1 (unset) the
 // built-in choice.
 int ln_warp_override();
+// EDGE_OPS_LN_WARP_THREADS: threads per CTA of the one-warp-per-row
+// LayerNorm (32, 64, 128 or 256); 0 (unset) the built-in choice.
+int ln_warp_threads_override();
 // EDGE_OPS_QUAD_THREADS: threads per CTA of the four-threads-per-head path
 // (64, 128 or 256); 0 (unset) the built-in choice.
 int quad_threads_override();

@@ -683,6 +683,11 @@ def t1_latency(torch, ops, synth, device):
     gu = synth.glu_inputs(0, bf, 1, INTER)["gate_up"].to(device)
     og = torch.empty(1, INTER, dtype=bf, device=device)
     res["glu_silu_d9728"] = measure(lambda: ops.glu_act(gu, ops.SILU, out=og))
+    # the floor of a dependent launch: a 16-element quantize (one CTA, one
+    # load, one store) chained the same way
+    xq = torch.ones(16, dtype=bf, device=device)
+    oq = torch.empty(16, dtype=torch.uint8, device=device)
+    res["launch_floor_quantize_16"] = measure(lambda: ops.quantize_fp8(xq, 1.0, out=oq))
 
     # host cost of one eager call at T = 1 (no graph): validation, dispatch
     # and cudaLaunchKernelEx in the C library, called once through ctypes

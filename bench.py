@@ -505,16 +505,17 @@ def sweep(torch, ops, synth, device, peak):
         del g, fns
         return [round(us, 3), round(gbs, 1), round(gbs / peak, 4), "cold" if cold else "warm"]
 
-    # reference: torch's own device copy under the same method (read + write bytes)
+    # reference: torch's own device copy under the same method, keyed by the
+    # bytes it moves (read + write, MiB), spanning the sizes of the cases below
     out["torch_copy_reference"] = {}
-    for mb in (16, 64, 256):
-        n = mb * 2 ** 20 // 2
+    for mb in (4, 8, 16, 32, 64, 128, 256):
+        n = mb * 2 ** 20 // 4  # bf16 elements per side
         src0 = torch.randn(n, device=device, dtype=bf)
 
         def make(src0=src0):
             a, b = src0.clone(), torch.empty_like(src0)
             return lambda: b.copy_(a)
-        out["torch_copy_reference"][f"{mb}MB"] = timed(make, 2 * n * 2)
+        out["torch_copy_reference"][f"{mb}MiB"] = timed(make, 2 * n * 2)
         del src0
     # QK-norm+RoPE, text profile (head_dim 256, rotary 64, out of place)
     for (hq, hk) in ((16, 2), (24, 4)):

@@ -210,5 +210,11 @@ __device__ __forceinline__ void prefetch_l2_line(const void* p) {
     if (p != nullptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
+// Prefetch into this SM's L1 the line holding *p, which must lie inside an
+// allocation (only issued after the kernel's wait, for data it will load).
+__device__ __forceinline__ void prefetch_l1_line(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p) : "memory");
+}
+
 
 }  // namespace edge

@@ -113,6 +113,11 @@ int glu_unroll_override() {
     return v;
 }
 
+int quant_unroll_override() {
+    static const int v = env_choice("EDGE_OPS_QUANT_UNROLL", {1, 2, 4});
+    return v;
+}
+
 }  // namespace edge
 
 namespace {

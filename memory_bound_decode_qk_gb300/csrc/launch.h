@@ -104,11 +104,13 @@ bool pdl_enabled();
 
 // Launch-shape overrides for tuning (0: the built-in choice), read once from
 // EDGE_OPS_QK_PATH (1: one head per lane group, 3: four threads per head),
-// EDGE_OPS_ROWS_VT (target vectors per thread: 1, 2, 4 or 8) and
-// EDGE_OPS_GLU_UNROLL (vectors per thread: 1, 2 or 4).
+// EDGE_OPS_ROWS_VT (target vectors per thread: 1, 2, 4 or 8),
+// EDGE_OPS_GLU_UNROLL and EDGE_OPS_QUANT_UNROLL (vectors per thread: 1, 2 or
+// 4).
 int qk_path_override();
 int rows_vt_override();
 int glu_unroll_override();
+int quant_unroll_override();
 // EDGE_OPS_LN_WARP: 1 one warp per LayerNorm row, 0 never; -1 (unset) the
 // built-in choice.
 int ln_warp_override();

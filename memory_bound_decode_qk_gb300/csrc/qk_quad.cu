@@ -211,6 +211,17 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
         const QuadUnit& un = h.un;
         const bool active = h.active, isv = h.isv;
         const int64_t pos = h.pos;
+        const bool rot = RQ > 0 && pos >= 0 && pos < p.cache_len;
+        if (rot) {
+            // the cos/sin lines of the rotated chunks into L1 now, so that
+            // their round trip overlaps the normalization below
+#pragma unroll
+            for (int i = 0; i < (RQ > 0 ? RQ : 1); ++i) {
+                const int64_t e = pos * p.half + (kt + K * i) * (LAYOUT == kInterleaved ? N / 2 : N);
+                prefetch_l1_line(p.cs + e);
+                prefetch_l1_line(p.sn + e);
+            }
+        }
         // beyond 32 terms per thread, two running sums alternating by chunk
         // (at most 4N sequential terms each, for the error bound of the
         // tolerance)
@@ -272,7 +283,6 @@ __device__ __forceinline__ void quad_body(const QKP& p, const Map& map) {
             }
         };
 
-        const bool rot = RQ > 0 && pos >= 0 && pos < p.cache_len;
         if (!active || (Map::kHasV && un.dst == nullptr)) return;
         char* out = un.dst;
         auto emit = [&](int i, const float (&y)[N]) {

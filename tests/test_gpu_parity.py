@@ -684,7 +684,8 @@ def test_layernorm_fp8_and_in_place(name):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
-@pytest.mark.parametrize("n,mis", [(1, 0), (8 * 1000 + 5, 0), (3 * 2 ** 20, 0), (77, 1)])
+@pytest.mark.parametrize("n,mis", [(1, 0), (8 * 1000 + 5, 0), (3 * 2 ** 20, 0),
+                                   (8 * 131109 + 3, 0), (77, 1)])
 def test_quantize_fp8(dtype, n, mis):
     fmt = TORCH_FMT[dtype]
     x = synth.to_dtype(synth.with_outliers(synth.normal(0, 51, n, 0.0, 1.0), 0, 52, 0.001, 20.0),

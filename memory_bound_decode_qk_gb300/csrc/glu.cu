@@ -51,9 +51,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float rcp_approx(float x) {
+// Reciprocal of x in [1, 2] (its only use: 1 / (1 + e^-|v|)).  Neither x nor
+// 1/x is subnormal there, so the flush-to-zero form gives the same result
+// without the subnormal handling of the plain form (measured on GB300: 1.17x
+// on the issue-bound tanh-GELU gate with FP8 output).
+__device__ __forceinline__ float rcp_approx_1to2(float x) {
     float y;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -69,7 +73,7 @@ __device__ __forceinline__ float gate_fast(float g, float u) {
     }
     const float t = ex2_approx(__fmul_rn(-fabsf(v), kLog2e));
     const float num = v >= 0.0f ? 1.0f : t;
-    return __fmul_rn(__fmul_rn(g, u), __fmul_rn(num, rcp_approx(__fadd_rn(1.0f, t))));
+    return __fmul_rn(__fmul_rn(g, u), __fmul_rn(num, rcp_approx_1to2(__fadd_rn(1.0f, t))));
 }
 
 // act(g) * u, accurate form (fp32 outputs).

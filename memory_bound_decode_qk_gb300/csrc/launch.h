@@ -98,8 +98,9 @@ int resident_ctas(const void* fn, int threads);
 
 // Programmatic dependent launch for all ops (on unless EDGE_OPS_PDL=0 in the
 // environment, read once per process).  Every kernel executes
-// griddepcontrol.wait before its first global access, so it is always safe as
-// a dependent; it triggers its own dependents at its start.
+// griddepcontrol.wait before its first global load whose value it uses, so
+// it is always safe as a dependent; it triggers its own dependents at its
+// start.
 bool pdl_enabled();
 
 // Launch-shape overrides for tuning (0: the built-in choice), read once from

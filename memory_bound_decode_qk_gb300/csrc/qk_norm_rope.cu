@@ -46,9 +46,21 @@ __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
         const uint32_t per_cta = (blockDim.x >> 5) * HPW;
         prefetch_heads(p, blockIdx.x * per_cta, (blockIdx.x + 1) * per_cta, true);
     }
+    // The first pass's position, read before the wait as an address hint for
+    // the cache row.  The preceding grid may still be writing it, so it is
+    // read at L2 (leaving no L1 line behind) and never used as a value: the
+    // row it names is loaded after the wait, next to the position itself,
+    // and kept only if the two positions agree (reloaded otherwise).  The
+    // position and the row then cost one round trip instead of two.
+    int64_t hint = -1;
+    if (p.rot > 0 && warp * HPW + slot < p.units) {
+        hint = __ldcg(reinterpret_cast<const long long*>(p.pos) +
+                      fast_div(warp * HPW + slot, p.heads));
+    }
     pdl_wait();
     pdl_launch_dependents();
 
+    const int lane_role = p.rot > 0 ? rotary_role<T, LAYOUT>(p, sub) : 0;
     for (uint32_t base = warp * HPW; base < p.units; base += nwarps * HPW) {
         const uint32_t u = base + slot;
         const bool active = u < p.units;
@@ -59,12 +71,15 @@ __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
             raw = __ldcs(reinterpret_cast<const uint4*>(un.src) + sub);
             if (p.rot > 0) pos = __ldg(p.pos + un.t);
         }
+        CacheRegs<T, LAYOUT> cr;
+        const bool hinted = lane_role != 0 && active && hint >= 0 && hint < p.cache_len;
+        if (hinted) load_cache<T, LAYOUT>(p, hint, sub, lane_role, cr);
         float w[N];
         weights_plus_delta<T>(p, un.w, sub, w);
         const bool rot = active && pos >= 0 && pos < p.cache_len;
-        const int role = rot ? rotary_role<T, LAYOUT>(p, sub) : 0;
-        CacheRegs<T, LAYOUT> cr;
-        if (role != 0) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
+        const int role = rot ? lane_role : 0;
+        if (role != 0 && !(hinted && pos == hint)) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
+        hint = -1;  // later passes take no hint
         qk_core<T, FP8, LPH, LAYOUT>(p, un.dst, active, lane, sub, raw, w, role, cr);
     }
 }

@@ -582,8 +582,9 @@ double quad_min_waves(int elem_bytes, int layout, int rotary_dim, int64_t head_b
 
 bool quad_suits(int layout, int rotary_dim, int64_t head_bytes) {
     // 512-byte heads in the interleaved layout need the two-CTA register
-    // budget, and measured no faster than the lane-group path at any width
-    // on GB300
+    // budget.  Measured on GB300, this path then wins at some widths and
+    // loses at others, by up to 15% each way (every partial wave of its grid
+    // costs a full pass), so the lane-group path keeps them.
     return !(layout == kInterleaved && rotary_dim > 0 && head_bytes == 512);
 }
 

@@ -46,9 +46,18 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
             prefetch_l2(p.q, t0 * a.row_bytes, t1 * a.row_bytes);
         }
     }
+    // The first pass's position as an address hint for the cache row, read
+    // before the wait at L2 and checked after it (as in the prologue's
+    // lane-group kernel): one round trip for the position and the row.
+    int64_t hint = -1;
+    if (p.rot > 0 && warp * HPW + slot_in_warp < p.units) {
+        hint = __ldcg(reinterpret_cast<const long long*>(p.pos) +
+                      fast_div(warp * HPW + slot_in_warp, a.per_token));
+    }
     pdl_wait();
     pdl_launch_dependents();
 
+    const int lane_role = p.rot > 0 ? rotary_role<T, LAYOUT>(p, sub) : 0;
     for (uint32_t base = warp * HPW; base < p.units; base += nwarps * HPW) {
         const uint32_t u = base + slot_in_warp;
         const bool active = u < p.units;
@@ -66,6 +75,10 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
             if (p.rot > 0 && !isv) pos = __ldg(p.pos + t);
             if (!isq && a.slots != nullptr) slot = __ldg(a.slots + t);
         }
+        CacheRegs<T, LAYOUT> cr;
+        const bool hinted =
+            lane_role != 0 && active && !isv && hint >= 0 && hint < p.cache_len;
+        if (hinted) load_cache<T, LAYOUT>(p, hint, sub, lane_role, cr);
         char* dst = nullptr;
         if (isq) {
             dst = p.qo + ((int64_t)t * p.q_heads + j) * hb;
@@ -75,9 +88,9 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
         float w[N];
         weights_plus_delta<T>(p, isq ? p.wq : p.wk, sub, w);
         const bool rot = active && !isv && pos >= 0 && pos < p.cache_len;
-        const int role = rot ? rotary_role<T, LAYOUT>(p, sub) : 0;
-        CacheRegs<T, LAYOUT> cr;
-        if (role != 0) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
+        const int role = rot ? lane_role : 0;
+        if (role != 0 && !(hinted && pos == hint)) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
+        hint = -1;  // later passes take no hint
         qk_core<T, false, LPH, LAYOUT>(p, dst, active && dst != nullptr, lane, sub, raw, w, role,
                                        cr, isv);
     }

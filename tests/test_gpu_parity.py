@@ -305,6 +305,91 @@ def test_qk_out_of_cache_token_untouched_by_rotation():
     assert okq.all()
 
 
+@pytest.mark.parametrize("T", [4, 1500])
+def test_qk_without_cache_rows_rotates_nothing(T):
+    # cache_len 0 with a rotary width: positions and cache are NULL and no
+    # token rotates, so the outputs equal those of rotary width 0 bit for bit
+    # (T = 4 takes the lane-group path, T = 1500 four threads per head)
+    inp = synth.qk_inputs(0, torch.bfloat16, T, 16, 2, 256, 0, theta=1e7, cache_len=0,
+                          positions="arange", w_std=0.05)
+    q, k, wq, wk = dev(inp["q"]), dev(inp["k"]), dev(inp["wq"]), dev(inp["wk"])
+    a = edge_ops.qk_norm_rope(q, k, wq, wk, None, None, None, rotary_dim=64, cache_len=0,
+                              weight_offset=1)
+    b = edge_ops.qk_norm_rope(q, k, wq, wk, None, None, None, rotary_dim=0, weight_offset=1)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def _position_delta_bf16(old, new):
+    """bf16 words that a residual add turns `old` positions into `new` ones.
+
+    An int64 position k < 256 is the little-endian words [k, 0, 0, 0], and the
+    bf16 word k is the value k * 2^-133 (subnormal below 128, exponent 1 from
+    128 to 255).  So adding the words [new - old, 0, 0, 0] in fp32 gives the
+    new position exactly."""
+    d = (new - old).astype(np.int64)
+    w = np.zeros((len(old), 4), np.uint16)
+    w[:, 0] = np.where(d >= 0, d, 0x8000 | -d).astype(np.uint16)
+    return torch.from_numpy(w.reshape(-1).view(np.int16).copy()).view(torch.bfloat16).view(1, -1)
+
+
+@pytest.mark.parametrize("op", ["qk", "qkv"])
+def test_positions_rewritten_by_the_preceding_kernel(op):
+    # The prologue's lane-group kernels read each token's position before
+    # their dependent-launch wait, as an address hint only, and check it
+    # after the wait.  Here the kernel just before them on the stream (a
+    # residual add whose residual is the positions array) rewrites the
+    # positions while the prologue may already be resident: a stale hint
+    # must cost a reload, never a wrong row.
+    T, Hq, Hk, D, rot, P = 12, 16, 2, 256, 64, 200
+    old = np.array([5, 6, 7, 250, 9, 10, 11, 12, 13, 14, 15, 16], np.int64)
+    new = np.array([7, 6, 201, 3, 100, 10, 0, 199, 13, 255, 1, 2], np.int64)
+    inp = synth.qk_inputs(0, torch.bfloat16, T, Hq, Hk, D, rot, theta=1e7, cache_len=P,
+                          positions=new, w_std=0.05)
+    fmt = oracle.BF16
+    pos = dev(torch.from_numpy(old))
+    cs, sn = dev(inp["cos"]), dev(inp["sin"])
+    wq, wk = dev(inp["wq"]), dev(inp["wk"])
+    delta = dev(_position_delta_bf16(old, new))
+    scratch = torch.empty_like(delta)
+    if op == "qk":
+        ref = oracle.qk_norm_rope(storage(inp["q"]), storage(inp["k"]), storage(inp["wq"]),
+                                  storage(inp["wk"]), fmt, rot, oracle.ROTATE_HALF, new,
+                                  storage(inp["cos"]), storage(inp["sin"]), 1e-6, 1, eta=ETA_NORM)
+        q, k = dev(inp["q"]), dev(inp["k"])
+        qo, ko = torch.empty_like(q), torch.empty_like(k)
+        edge_ops.add_rmsnorm(delta, pos.view(torch.bfloat16).view(1, -1), None, out=scratch)
+        edge_ops.qk_norm_rope(q, k, wq, wk, pos, cs, sn, rotary_dim=rot, weight_offset=1,
+                              q_out=qo, k_out=ko)
+        torch.cuda.synchronize()
+        assert np.array_equal(pos.cpu().numpy(), new)
+        check_out("q", storage(qo.cpu()), ref.q_out, ref.q_pre, ref.q_mag, fmt, fmt, ETA_NORM,
+                  lo=ref.q_lo, hi=ref.q_hi)
+        check_out("k", storage(ko.cpu()), ref.k_out, ref.k_pre, ref.k_mag, fmt, fmt, ETA_NORM,
+                  lo=ref.k_lo, hi=ref.k_hi)
+        return
+    qkv = torch.cat([inp["q"].reshape(T, -1), inp["k"].reshape(T, -1),
+                     inp["k"].reshape(T, -1)], dim=1).contiguous()
+    slots = np.arange(T, dtype=np.int64)
+    z = np.zeros((T, Hk, D), np.uint16)
+    ref = oracle.qkv_rope_cache(storage(qkv), storage(inp["wq"]), storage(inp["wk"]), fmt, Hq,
+                                Hk, rot, oracle.ROTATE_HALF, new, storage(inp["cos"]),
+                                storage(inp["sin"]), slots, z, z, 1e-6, 1, 1, eta=ETA_NORM)
+    kc = torch.zeros(T, Hk, D, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    qo = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
+    edge_ops.add_rmsnorm(delta, pos.view(torch.bfloat16).view(1, -1), None, out=scratch)
+    edge_ops.qkv_rope_cache(dev(qkv), Hq, Hk, wq, wk, pos, cs, sn, dev(torch.from_numpy(slots)),
+                            kc, vc, rotary_dim=rot, weight_offset=1, q_out=qo)
+    torch.cuda.synchronize()
+    assert np.array_equal(pos.cpu().numpy(), new)
+    check_out("q", storage(qo.cpu()), ref.q_out, ref.q_pre, ref.q_mag, fmt, fmt, ETA_NORM,
+              lo=ref.q_lo, hi=ref.q_hi)
+    check_out("k_cache", storage(kc.cpu()), ref.k_cache, ref.k_pre, ref.k_mag, fmt, fmt,
+              ETA_NORM, lo=ref.k_lo, hi=ref.k_hi)
+    assert np.array_equal(storage(vc.cpu()), ref.v_cache)
+
+
 # ---------------------------------------------------------------- rows
 
 ROW_CASES = {

@@ -16,6 +16,9 @@
 //   - The rotate-half partner vector sits half/N lanes away and comes over a
 //     shuffle.  Interleaved pairs sit inside one vector.
 //   - cos/sin entries are read from L1: every head of a token shares the row.
+//   - The row is loaded at a position hint read before the dependent-launch
+//     wait, next to the position itself, and reloaded only if they differ:
+//     one round trip for the position and its row.
 // Units are ordered token-major, so the warps of a CTA share cos/sin rows and
 // the norm weights.  Streamed inputs use evict-first loads.
 // Many heads: the four-threads-per-head path (qk_quad.cu) takes over past a

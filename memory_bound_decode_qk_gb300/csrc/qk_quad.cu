@@ -26,7 +26,8 @@
 //     HVQ chunks their partners; for the interleaved layout, pairs lie inside
 //     a chunk.
 // The rotated chunk count RQ is a template parameter, so every chunk's role is
-// known at compile time.  About 50 warp-instructions per head remain.  All C
+// known at compile time.  A head's cos/sin lines are prefetched into L1 as its
+// arithmetic begins, so the rotation reads them without another round trip.  About 50 warp-instructions per head remain.  All C
 // loads of a thread are issued before any arithmetic, so a warp (8 heads) has
 // 4 KB in flight.
 //

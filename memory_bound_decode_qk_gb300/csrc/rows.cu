@@ -500,6 +500,11 @@ bool vec_shape(const RowsArgs& a, int sms, RowsP& p, int& V) {
     // one input stream per row (plain RMSNorm): more vectors per thread keep
     // enough bytes in flight once there are many rows (measured on GB300)
     if (!a.residual && !a.layernorm && a.rows >= 8 * sms) vt = 4;
+    // at most 8 warps per row: wider rows take two vectors per thread, which
+    // halves the CTA and the cross-warp combine (measured on GB300: the
+    // decode step at hidden 2560 and T = 64 4% faster, its row launches alone
+    // within 2%, and hidden 4096 at T = 64 6% faster)
+    if (vt == 1 && nvec > 8 * 32) vt = 2;
     if (rows_vt_override() > 0) vt = rows_vt_override();
     int W = (int)((nvec + 32 * vt - 1) / (32 * vt));
     if (W > 16) W = 16;

@@ -102,3 +102,16 @@ def f32_ok(got: np.ndarray, pre: np.ndarray, mag: np.ndarray, rel: float,
 def report(name: str, ok: np.ndarray) -> str:
     bad = np.flatnonzero(~ok.ravel())
     return f"{name}: {bad.size} of {ok.size} outside tolerance; first at {bad[:8].tolist()}"
+
+
+def position_delta_bf16(old, new):
+    """bf16 words that a residual add turns `old` positions into `new` ones.
+
+    An int64 position k < 256 is the little-endian words [k, 0, 0, 0], and the
+    bf16 word k is the value k * 2^-133 (subnormal below 128, exponent 1 from
+    128 to 255).  So adding the words [new - old, 0, 0, 0] in fp32 gives the
+    new position exactly."""
+    d = (new - old).astype(np.int64)
+    w = np.zeros((len(old), 4), np.uint16)
+    w[:, 0] = np.where(d >= 0, d, 0x8000 | -d).astype(np.uint16)
+    return torch.from_numpy(w.reshape(-1).view(np.int16).copy()).view(torch.bfloat16).view(1, -1)

@@ -26,7 +26,8 @@ import pytest
 import torch
 
 import oracle
-from helpers import TORCH_FMT, f32_ok, report, storage, strict_ok, ulp_distance, within_one_ulp
+from helpers import (TORCH_FMT, f32_ok, position_delta_bf16, report, storage, strict_ok,
+                     ulp_distance, within_one_ulp)
 from memory_bound_decode_qk_gb300 import edge_ops, synth
 
 pytestmark = pytest.mark.gpu
@@ -320,19 +321,6 @@ def test_qk_without_cache_rows_rotates_nothing(T):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def _position_delta_bf16(old, new):
-    """bf16 words that a residual add turns `old` positions into `new` ones.
-
-    An int64 position k < 256 is the little-endian words [k, 0, 0, 0], and the
-    bf16 word k is the value k * 2^-133 (subnormal below 128, exponent 1 from
-    128 to 255).  So adding the words [new - old, 0, 0, 0] in fp32 gives the
-    new position exactly."""
-    d = (new - old).astype(np.int64)
-    w = np.zeros((len(old), 4), np.uint16)
-    w[:, 0] = np.where(d >= 0, d, 0x8000 | -d).astype(np.uint16)
-    return torch.from_numpy(w.reshape(-1).view(np.int16).copy()).view(torch.bfloat16).view(1, -1)
-
-
 @pytest.mark.parametrize("op", ["qk", "qkv"])
 def test_positions_rewritten_by_the_preceding_kernel(op):
     # The prologue's lane-group kernels read each token's position before
@@ -350,7 +338,7 @@ def test_positions_rewritten_by_the_preceding_kernel(op):
     pos = dev(torch.from_numpy(old))
     cs, sn = dev(inp["cos"]), dev(inp["sin"])
     wq, wk = dev(inp["wq"]), dev(inp["wk"])
-    delta = dev(_position_delta_bf16(old, new))
+    delta = dev(position_delta_bf16(old, new))
     scratch = torch.empty_like(delta)
     if op == "qk":
         ref = oracle.qk_norm_rope(storage(inp["q"]), storage(inp["k"]), storage(inp["wq"]),

@@ -400,6 +400,8 @@ ROW_CASES = {
                                          w_std=0.1, off=1, misalign=1),
     "generic_h40000": dict(dtype=torch.bfloat16, T=2, H=40000, w_mean=1.0, w_std=0.1, off=0),
     "no_weight_h2048": dict(dtype=torch.bfloat16, T=128, H=2048, w_mean=None, w_std=0.0, off=0),
+    # a row of 512 vectors at few rows: two vectors per thread, 8 warps per row
+    "h4096_T64_offset": dict(dtype=torch.bfloat16, T=64, H=4096, w_mean=0.0, w_std=0.02, off=1),
 }
 
 
@@ -459,7 +461,8 @@ def test_rows(name, fused):
     run_rows(ROW_CASES[name], fused)
 
 
-@pytest.mark.parametrize("name", ["cfg2_h2560_T4_offset", "h2048_T512", "generic_h37"])
+@pytest.mark.parametrize("name", ["cfg2_h2560_T4_offset", "cfg2_h2560_T64_direct", "h2048_T512",
+                                  "generic_h37"])
 @pytest.mark.parametrize("fused", [True, False])
 def test_rows_in_place(name, fused):
     c = ROW_CASES[name]
@@ -482,6 +485,9 @@ FP8_ROWS = {
                           outliers=0.001),
     "f32_h1024": dict(dtype=torch.float32, T=77, H=1024, w_mean=1.0, w_std=0.1, off=0),
     "generic_h37": dict(dtype=torch.bfloat16, T=64, H=37, w_mean=1.0, w_std=0.1, off=0),
+    # the decode width with the FP8 epilogue: two vectors per thread, 5 warps per row
+    "h2560_T64": dict(dtype=torch.bfloat16, T=64, H=2560, w_mean=1.0, w_std=0.02, off=0,
+                      outliers=0.001),
 }
 
 

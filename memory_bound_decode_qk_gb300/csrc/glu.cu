@@ -238,7 +238,8 @@ cudaError_t launch_typed(const GluArgs& a, GluP& p, cudaStream_t s) {
         p.total = (uint32_t)(a.rows * dvec);
         const int threads = 256;
         // one vector per thread and a one-shot grid (measured on GB300: 2 or 4
-        // vectors per thread were slower at every size)
+        // vectors per thread were slower at every size timed on its own,
+        // 1.1x to 1.2x for the tanh-GELU gate with FP8 output)
         int U = 1;
         if (glu_unroll_override() > 0) U = glu_unroll_override();
         int64_t blocks = ((int64_t)p.total + threads * U - 1) / (threads * U);

@@ -73,6 +73,8 @@ def _lib():
         L.oracle_qkv_rope_cache.argtypes = [P] * 14 + [I, I64, I, I, I, I, I, P, P, P, I64, P, I64,
                                                          F, I, I, D]
         L.oracle_set_rotation_scale.argtypes = [D]
+        L.oracle_near_tie.argtypes = [D, I, D, ctypes.POINTER(D)]
+        L.oracle_near_tie.restype = ctypes.c_int
         for name in ("oracle_rmsnorm", "oracle_add_rmsnorm", "oracle_glu_act", "oracle_rope",
                      "oracle_qk_norm_rope", "oracle_layernorm", "oracle_quantize_static",
                      "oracle_qkv_rope_cache",
@@ -113,6 +115,16 @@ def bits_of(v, fmt: int) -> int:
 
 def value_of(bits: int, fmt: int) -> float:
     return _lib().oracle_value(int(bits), fmt)
+
+
+def near_tie(v, fmt: int, eta: float):
+    """The tie policy's decision for one exact value: (flagged, other), where
+    flagged says the rounding of v to fmt lies within the relative band eta of
+    a rounding boundary and other is the neighbour across it (v's own rounding
+    when not flagged)."""
+    o = ctypes.c_double(0.0)
+    t = _lib().oracle_near_tie(float(v), fmt, float(eta), ctypes.byref(o))
+    return bool(t), o.value
 
 
 def decode(a: np.ndarray, fmt: int) -> np.ndarray:

@@ -508,6 +508,17 @@ static int near_tie(double v, int f, double eta, double* other)
     return 1;
 }
 
+/* Test hook: the near-tie decision of the tie policy for one value v (1 when
+ * its rounding to f is decided within the relative band eta; *other then
+ * receives the neighbour on the far side of the boundary, else v's rounding). */
+int oracle_near_tie(double v, int f, double eta, double* other)
+{
+    double o = oracle_round(v, f);
+    int t = near_tie(v, f, eta, &o);
+    if (other) *other = o;
+    return t;
+}
+
 /* `heads` heads of D elements read from x at element offset x_off and
  * written to out (and the diagnostics) at element offset out_off; without
  * `normalize` the head passes through unnormalized (standalone rotation, or

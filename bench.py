@@ -69,7 +69,47 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-t1", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=6.0)
+    # --probe: launch one op (or the whole sweep) a few times for a profiler to
+    # capture; no timing, no JSON line
+    ap.add_argument("--probe", metavar="OP", choices=PROBE_OPS + ("sweep",))
+    ap.add_argument("--T", type=int, default=2048)
+    ap.add_argument("--hq", type=int, default=16)
+    ap.add_argument("--hk", type=int, default=2)
+    ap.add_argument("--d", type=int, default=256)
+    ap.add_argument("--rot", type=int, default=64)
+    ap.add_argument("--hidden", type=int, default=2048)
+    ap.add_argument("--inter", type=int, default=9728)
+    ap.add_argument("--fp8", action="store_true")
+    ap.add_argument("--no-weight", action="store_true")
+    ap.add_argument("--reps", type=int, default=3)
     return ap.parse_args()
+
+
+PROBE_OPS = ("qk", "qk_dflash2", "add_rmsnorm", "rmsnorm", "rope", "layernorm", "quantize",
+             "qkv_cache", "glu_silu", "glu_gelu", "copy")
+
+
+def run_probe(args):
+    """Launch one op (or every case of the sweep) `reps` times on cuda:0,
+    through the C ABI, for ncu to capture."""
+    import torch
+
+    from memory_bound_decode_qk_gb300 import edge_ops as ops, synth
+
+    ops.lib()
+    if args.probe == "sweep":
+        cases = [(op, dict(kw, T=T)) for _, op, kw, Ts in SWEEP for T in Ts]
+    else:
+        cases = [(args.probe, dict(T=args.T, hq=args.hq, hk=args.hk, d=args.d, rot=args.rot,
+                                   hidden=args.hidden, inter=args.inter, fp8=args.fp8,
+                                   weight=not args.no_weight))]
+    for op, kw in cases:
+        fn = probe_case(torch, ops, synth, op, torch.bfloat16, **kw)
+        for _ in range(args.reps):
+            fn()
+        torch.cuda.synchronize()
+        print(op, kw, "ok", flush=True)
+    return 0
 
 
 # ---------------------------------------------------------------- bytes
@@ -300,34 +340,57 @@ def cpu_baseline(seconds):
                       f"{el1:.1f} s on one thread; the C fp64 oracle on the host"}
 
 
+def step_config(world):
+    """The workload description both arms report."""
+    step_bytes = LAYERS * layer_bytes()
+    return {"workload": "decode seams of a 36-layer decoder: per layer add_rmsnorm, "
+                        "qk_norm_rope, add_rmsnorm, silu_and_mul",
+            "T": T_DEC, "hidden": HID, "gate": INTER, "heads": [HQ, HK], "head_dim": HD,
+            "rotary": [HD, "rotate_half"], "layers": LAYERS, "global_batch": T_DEC * world,
+            "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB per step, "
+                  "distinct buffers per layer",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
+    """The oracle as it stands, on the host cores, on the benchmark's own step:
+    the layers of a step (T = 64) split over the host threads, one layer per
+    thread at a time.  A step takes all 36 layers when K + W steps of them fit
+    in about two minutes; otherwise each step takes the largest whole number
+    of layers that does (at least one per thread)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     from concurrent.futures import ThreadPoolExecutor
 
-    T = 8  # bounded sample: 8 tokens of a layer per host thread per step
-    a = oracle_layer_args(T)
+    a = oracle_layer_args(T_DEC)
     cores, model = cpu_info()
+    t0 = time.perf_counter()
+    oracle_layer(a)
+    t_layer = time.perf_counter() - t0
+    total = args.steps + args.warmup
+    per_step = LAYERS
+    if total * per_step * t_layer / cores > 120.0:
+        per_step = max(cores, int(120.0 * cores / (total * t_layer)) // cores * cores)
+        per_step = min(per_step, LAYERS)
     with ThreadPoolExecutor(cores) as ex:
         def step():
-            list(ex.map(lambda _: oracle_layer(a), range(cores)))
+            list(ex.map(lambda _: oracle_layer(a), range(per_step)))
         for _ in range(args.warmup):
             step()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             step()
         el = time.perf_counter() - t0
-    gbs = cores * layer_bytes(T) * args.steps / el / 1e9
-    sample = (f"{T} tokens of one layer (4 ops) on each of {cores} host threads per step; "
-              f"the C fp64 oracle ({model})")
+    gbs = layer_bytes() * per_step * args.steps / el / 1e9
+    sample = (f"{per_step} of the step's {LAYERS} layers (T={T_DEC}, 4 ops each) per step, on "
+              f"{cores} host threads (one layer each at a time); the C fp64 oracle ({model})")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "decode seams of a 36-layer decoder (reference arm: sample)",
-                   "T": T, "hidden": HID, "gate": INTER, "heads": [HQ, HK], "head_dim": HD},
+        "config": step_config(1),
         "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "cpu": model, "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -471,15 +534,149 @@ def traffic_for(kernel):
 
 # ---------------------------------------------------------------- sweep
 
+def probe_case(torch, ops, synth, op, dtype, T, hq=16, hk=2, d=256, rot=64, hidden=2048,
+               inter=9728, fp8=False, weight=True, device="cuda"):  # noqa: C901 (one branch per op)
+    """A zero-argument callable that launches one op once, on buffers of its own
+    (seeded synthetic inputs shaped like the workloads), through the C ABI."""
+    u8 = torch.uint8
+    if op == "qk":
+        i = synth.qk_inputs(0, dtype, T, hq, hk, d, rot, theta=1e7, cache_len=32768,
+                            positions="offset", w_std=0.05)
+        t = {k: (v.to(device) if v is not None else None) for k, v in i.items()}
+        qo = torch.empty(t["q"].shape, dtype=u8 if fp8 else dtype, device=device)
+        ko = torch.empty(t["k"].shape, dtype=u8 if fp8 else dtype, device=device)
+        return lambda: ops.qk_norm_rope(t["q"], t["k"], t["wq"], t["wk"], t["positions"],
+                                        t["cos"], t["sin"], rotary_dim=rot, weight_offset=1,
+                                        q_out=qo, k_out=ko, fp8=fp8, inv_scale=40.0)
+    if op == "qk_dflash2":
+        # DFlash2 pair: 32 + 32 heads of 128, full rotary, direct weights, in
+        # place; W = 16 draft positions per sequence
+        i = synth.qk_inputs(0, dtype, T, 32, 32, 128, 128, theta=1e6, cache_len=32768,
+                            positions="blocks:16", w_mean=1.0, w_std=0.02)
+        t = {k: v.to(device) for k, v in i.items()}
+        return lambda: ops.qk_norm_rope(t["q"], t["k"], t["wq"], t["wk"], t["positions"],
+                                        t["cos"], t["sin"], rotary_dim=128, q_out=t["q"],
+                                        k_out=t["k"])
+    if op in ("add_rmsnorm", "rmsnorm"):
+        i = synth.rows_inputs(0, dtype, T, hidden, residual=op == "add_rmsnorm")
+        x = i["x"].to(device)
+        w = i["w"].to(device) if weight else None
+        o = torch.empty(T, hidden, dtype=u8 if fp8 else dtype, device=device)
+        if op == "rmsnorm":
+            return lambda: ops.rmsnorm(x, w, eps=EPS, out=o, fp8=fp8, inv_scale=40.0)
+        r = i["residual"].to(device)
+        return lambda: ops.add_rmsnorm(x, r, w, eps=EPS, out=o, fp8=fp8, inv_scale=40.0)
+    if op == "rope":
+        i = synth.qk_inputs(0, dtype, T, hq, hk, d, rot, theta=1e7, cache_len=32768,
+                            positions="offset")
+        t = {k: (v.to(device) if v is not None else None) for k, v in i.items()}
+        qo, ko = torch.empty_like(t["q"]), torch.empty_like(t["k"])
+        return lambda: ops.rope(t["q"], t["k"], t["positions"], t["cos"], t["sin"],
+                                rotary_dim=rot, q_out=qo, k_out=ko)
+    if op == "layernorm":
+        i = synth.rows_inputs(0, dtype, T, hidden, residual=False)
+        x, g = i["x"].to(device), i["w"].to(device)
+        o = torch.empty(T, hidden, dtype=u8 if fp8 else dtype, device=device)
+        return lambda: ops.layernorm(x, g, g, eps=1e-6, out=o, fp8=fp8, inv_scale=40.0)
+    if op == "quantize":
+        x = synth.rows_inputs(0, dtype, T, hidden, residual=False)["x"].to(device)
+        o = torch.empty(x.shape, dtype=u8, device=device)
+        return lambda: ops.quantize_fp8(x, 40.0, out=o)
+    if op == "qkv_cache":
+        qkv = synth.to_dtype(synth.normal(0, 71, T * (hq + 2 * hk) * d), dtype).view(T, -1)
+        qkv = qkv.to(device)
+        w = synth.to_dtype(synth.normal(0, 72, d, 0.0, 0.05), dtype).to(device)
+        cos, sin = synth.rope_cache(1e7, rot, 32768)
+        cos, sin = cos.to(device), sin.to(device)
+        pos = torch.arange(T, dtype=torch.int64, device=device)
+        kc = torch.empty(T, hk, d, dtype=dtype, device=device)
+        vc = torch.empty_like(kc)
+        qo = torch.empty(T, hq, d, dtype=dtype, device=device)
+        return lambda: ops.qkv_rope_cache(qkv, hq, hk, w, w, pos, cos, sin, pos, kc, vc,
+                                          rotary_dim=rot, weight_offset=1, q_out=qo)
+    if op in ("glu_silu", "glu_gelu"):
+        gu = synth.glu_inputs(0, dtype, T, inter)["gate_up"].to(device)
+        o = torch.empty(T, inter, dtype=u8 if fp8 else dtype, device=device)
+        act = ops.SILU if op == "glu_silu" else ops.GELU_TANH
+        return lambda: ops.glu_act(gu, act, out=o, fp8=fp8, inv_scale=40.0)
+    if op == "copy":
+        # the yardstick: `hidden` bytes moved, half read and half written
+        src = torch.zeros(hidden // 2, dtype=u8, device=device)
+        dst = torch.empty_like(src)
+        return lambda: ops.copy(src, out=dst)
+    raise ValueError(op)
+
+
+def case_bytes(op, T, hq=16, hk=2, d=256, rot=64, hidden=2048, inter=9728, fp8=False,
+               weight=True):
+    """Algorithmic bytes of one call of a probe case."""
+    o = 1 if fp8 else 2
+    if op == "qk":
+        return bytes_qk(T, hq, hk, d, rot, out_s=o)
+    if op == "qk_dflash2":
+        return bytes_qk(T, 32, 32, 128, 128)
+    if op == "add_rmsnorm":
+        return bytes_add_rmsnorm(T, hidden, out_s=o, weight=weight)
+    if op == "rmsnorm":
+        return bytes_rmsnorm(T, hidden, out_s=o, weight=weight)
+    if op == "rope":
+        return bytes_rope(T, hq, hk, d, rot)
+    if op == "layernorm":
+        return bytes_layernorm(T, hidden, out_s=o)
+    if op == "quantize":
+        return bytes_quant(T * hidden)
+    if op == "qkv_cache":
+        return bytes_qkv_cache(T, hq, hk, d, rot)
+    if op in ("glu_silu", "glu_gelu"):
+        return bytes_glu(T, inter, out_s=o)
+    if op == "copy":
+        return hidden
+    raise ValueError(op)
+
+
+# The sweep: (key, op, fixed arguments, values of T).  Every op has a T = 256
+# point, the width at which the ops should reach 70% of HBM peak.
+SWEEP = [
+    ("qk_norm_rope_bf16_16x2_d256_r64", "qk", dict(hq=16, hk=2),
+     (1, 8, 32, 128, 256, 512, 1024, 2048)),
+    ("qk_norm_rope_bf16_24x4_d256_r64", "qk", dict(hq=24, hk=4),
+     (1, 8, 32, 128, 256, 512, 1024, 2048)),
+    ("qk_norm_rope_dflash2_bf16_32x32_d128_inplace_W16", "qk_dflash2", {},
+     (16, 64, 256, 1024, 2048)),
+    ("add_rmsnorm_bf16_h2048", "add_rmsnorm", dict(hidden=2048), (1, 16, 64, 256, 512, 1024, 4096)),
+    ("add_rmsnorm_bf16_h2048_fp8", "add_rmsnorm", dict(hidden=2048, fp8=True),
+     (1, 16, 64, 256, 512, 1024, 4096)),
+    ("add_rmsnorm_bf16_h1024", "add_rmsnorm", dict(hidden=1024), (1, 16, 64, 256, 512, 1024, 4096)),
+    ("add_rmsnorm_bf16_h1024_fp8", "add_rmsnorm", dict(hidden=1024, fp8=True),
+     (1, 16, 64, 256, 512, 1024, 4096)),
+    ("add_rmsnorm_bf16_h2560", "add_rmsnorm", dict(hidden=2560), (1, 16, 64, 256, 512, 1024, 4096)),
+    ("add_rmsnorm_bf16_h2560_fp8", "add_rmsnorm", dict(hidden=2560, fp8=True),
+     (1, 16, 64, 256, 512, 1024, 4096)),
+    ("rmsnorm_noweight_bf16_h2048_fp8", "rmsnorm", dict(hidden=2048, fp8=True, weight=False),
+     (1, 64, 256, 512, 4096)),
+    ("rope_bf16_24x4_d256_r64", "rope", dict(hq=24, hk=4), (1, 64, 256, 512, 2048)),
+    ("layernorm_bf16_h1152", "layernorm", dict(hidden=1152), (1, 64, 256, 512, 4096)),
+    ("quantize_fp8_bf16_rows_x2048", "quantize", dict(hidden=2048), (1, 256, 512, 4096)),
+    ("qkv_rope_cache_bf16_16x2_d256_r64", "qkv_cache", dict(hq=16, hk=2), (1, 64, 256, 512, 2048)),
+    ("glu_silu_bf16_d9728", "glu_silu", dict(inter=9728), (1, 64, 256, 512, 4096)),
+    ("glu_gelu_bf16_d2048_fp8", "glu_gelu", dict(inter=2048, fp8=True), (1, 64, 256, 512, 4096)),
+    ("glu_gelu_bf16_d10240", "glu_gelu", dict(inter=10240), (1, 64, 256, 512, 4096)),
+]
+
+
 def sweep(torch, ops, synth, device, peak):
-    """Per-op time vs T.  S copies of the call's buffers, with S * bytes over
-    2.5x L2 where that fits in 64 copies, are cycled by a graph of at least 32
-    back-to-back launches, so every launch reads cold inputs from HBM.  The
-    graph is replayed 10 times after 3 warm-ups and timed with events.  Below
-    that size the data stays L2-resident, and the entry is marked warm."""
+    """Per-op time vs T, each beside the yardstick copy of the same bytes.
+
+    S copies of a call's buffers, with S * bytes over 2.5x L2 where that fits
+    in 64 copies, are cycled by a graph of at least 32 back-to-back launches,
+    so every launch reads cold inputs from HBM.  The graph is replayed 10
+    times after 3 warm-ups and timed with events.  Below that size the data
+    stays L2-resident, and the entry is marked warm.  The copy moves the op's
+    algorithmic bytes (half read, half written) with the ops' launch form
+    (edge_copy), timed the same way: its time is what a kernel that only moves
+    those bytes needs."""
     bf = torch.bfloat16
     stream = torch.cuda.Stream(device)
-    out = {}
 
     def timed(make, nbytes):
         sets = int(min(64, max(2, -(-int(2.5 * L2_BYTES) // nbytes))))
@@ -500,146 +697,38 @@ def sweep(torch, ops, synth, device, peak):
             b.record(stream)
         torch.cuda.synchronize()
         us = a.elapsed_time(b) * 1e3 / (10 * reps)
-        gbs = nbytes / (us * 1e-6) / 1e9
         cold = sets * nbytes >= 2 * L2_BYTES
         del g, fns
-        return [round(us, 3), round(gbs, 1), round(gbs / peak, 4), "cold" if cold else "warm"]
+        return us, cold
 
-    # reference: torch's own device copy under the same method, keyed by the
-    # bytes it moves (read + write, MiB), spanning the sizes of the cases below
-    out["torch_copy_reference"] = {}
-    for mb in (4, 8, 16, 32, 64, 128, 256):
-        n = mb * 2 ** 20 // 4  # bf16 elements per side
-        src0 = torch.randn(n, device=device, dtype=bf)
-
-        def make(src0=src0):
-            a, b = src0.clone(), torch.empty_like(src0)
-            return lambda: b.copy_(a)
-        out["torch_copy_reference"][f"{mb}MiB"] = timed(make, 2 * n * 2)
-        del src0
-    # QK-norm+RoPE, text profile (head_dim 256, rotary 64, out of place)
-    for (hq, hk) in ((16, 2), (24, 4)):
-        key = f"qk_norm_rope_bf16_{hq}x{hk}_d256_r64"
+    out = {}
+    for key, op, kw, Ts in SWEEP:
         out[key] = {}
-        for T in (1, 8, 32, 128, 256, 512, 1024, 2048):
-            i = synth.qk_inputs(0, bf, T, hq, hk, 256, 64, theta=1e7, cache_len=32768,
-                                positions="offset", w_std=0.05)
-            d = {k: v.to(device) for k, v in i.items()}
-
-            def make(d=d):
-                q, k = d["q"].clone(), d["k"].clone()
-                qo, ko = torch.empty_like(q), torch.empty_like(k)
-                return lambda: ops.qk_norm_rope(q, k, d["wq"], d["wk"], d["positions"], d["cos"],
-                                                d["sin"], rotary_dim=64, weight_offset=1,
-                                                q_out=qo, k_out=ko)
-            out[key][str(T)] = timed(make, bytes_qk(T, hq, hk, 256, 64))
-    # DFlash2 pair [128, 32, W, B]: 32 + 32 heads of 128, full rotary, direct
-    # weights, in place; W = 16 draft positions per sequence, B sequences
-    key = "qk_norm_rope_dflash2_bf16_32x32_d128_inplace_W16"
-    out[key] = {}
-    for B in (1, 4, 16, 64, 128):
-        T = 16 * B
-        i = synth.qk_inputs(0, bf, T, 32, 32, 128, 128, theta=1e6, cache_len=32768,
-                            positions="blocks:16", w_mean=1.0, w_std=0.02)
-        d = {k: v.to(device) for k, v in i.items()}
-
-        def make(d=d):
-            q, k = d["q"].clone(), d["k"].clone()
-            return lambda: ops.qk_norm_rope(q, k, d["wq"], d["wk"], d["positions"], d["cos"],
-                                            d["sin"], rotary_dim=128, weight_offset=0,
-                                            q_out=q, k_out=k)
-        out[key][f"B{B}"] = timed(make, bytes_qk(T, 32, 32, 128, 128))
-    # residual-add RMSNorm, bf16 out and FP8 out
-    for H in (2048, 1024, 2560):
-        for fp8 in (False, True):
-            key = f"add_rmsnorm_bf16_h{H}" + ("_fp8" if fp8 else "")
-            out[key] = {}
-            for T in (1, 16, 64, 256, 512, 1024, 4096):
-                i = synth.rows_inputs(0, bf, T, H)
-                x0, r0, w = (i[k].to(device) for k in ("x", "residual", "w"))
-
-                def make(x0=x0, r0=r0, w=w, T=T, H=H, fp8=fp8):
-                    x, r = x0.clone(), r0.clone()
-                    o = torch.empty(T, H, dtype=torch.uint8 if fp8 else bf, device=device)
-                    return lambda: ops.add_rmsnorm(x, r, w, eps=EPS, out=o, fp8=fp8,
-                                                   inv_scale=40.0)
-                out[key][str(T)] = timed(make, bytes_add_rmsnorm(T, H, out_s=1 if fp8 else 2))
-    key = "rmsnorm_noweight_bf16_h2048_fp8"
-    out[key] = {}
-    for T in (1, 64, 512, 4096):
-        x0 = synth.rows_inputs(0, bf, T, 2048, residual=False)["x"].to(device)
-
-        def make(x0=x0, T=T):
-            x = x0.clone()
-            o = torch.empty(T, 2048, dtype=torch.uint8, device=device)
-            return lambda: ops.rmsnorm(x, None, eps=EPS, out=o, fp8=True, inv_scale=40.0)
-        out[key][str(T)] = timed(make, bytes_rmsnorm(T, 2048, out_s=1, weight=False))
-    # standalone rotary, one-read LayerNorm, static FP8 quantize, fused QKV + KV write
-    key = "rope_bf16_24x4_d256_r64"
-    out[key] = {}
-    for T in (1, 64, 512, 2048):
-        i = synth.qk_inputs(0, bf, T, 24, 4, 256, 64, theta=1e7, cache_len=32768,
-                            positions="offset")
-        d = {k: v.to(device) for k, v in i.items() if v is not None}
-
-        def make(d=d):
-            q, k = d["q"].clone(), d["k"].clone()
-            qo, ko = torch.empty_like(q), torch.empty_like(k)
-            return lambda: ops.rope(q, k, d["positions"], d["cos"], d["sin"], rotary_dim=64,
-                                    q_out=qo, k_out=ko)
-        out[key][str(T)] = timed(make, bytes_rope(T, 24, 4, 256, 64))
-    key = "layernorm_bf16_h1152"
-    out[key] = {}
-    for T in (1, 64, 512, 4096):
-        i = synth.rows_inputs(0, bf, T, 1152)
-        x0, g = i["x"].to(device), i["w"].to(device)
-
-        def make(x0=x0, g=g):
-            x = x0.clone()
-            o = torch.empty_like(x)
-            return lambda: ops.layernorm(x, g, g, eps=1e-6, out=o)
-        out[key][str(T)] = timed(make, bytes_layernorm(T, 1152))
-    key = "quantize_fp8_bf16_rows_x2048"
-    out[key] = {}
-    for T in (1, 512, 4096):
-        x0 = synth.rows_inputs(0, bf, T, 2048, residual=False)["x"].to(device)
-
-        def make(x0=x0):
-            x = x0.clone()
-            o = torch.empty(x.shape, dtype=torch.uint8, device=device)
-            return lambda: ops.quantize_fp8(x, 40.0, out=o)
-        out[key][str(T)] = timed(make, bytes_quant(T * 2048))
-    key = "qkv_rope_cache_bf16_16x2_d256_r64"
-    out[key] = {}
-    for T in (1, 64, 512, 2048):
-        qkv0 = synth.to_dtype(synth.normal(0, 71, T * 20 * 256), bf).view(T, -1).to(device)
-        w = synth.to_dtype(synth.normal(0, 72, 256, 0.0, 0.05), bf).to(device)
-        cos, sin = synth.rope_cache(1e7, 64, 32768)
-        cos, sin = cos.to(device), sin.to(device)
-        pos = torch.arange(T, dtype=torch.int64, device=device)
-
-        def make(qkv0=qkv0, w=w, cos=cos, sin=sin, pos=pos, T=T):
-            qkv = qkv0.clone()
-            kc = torch.empty(T, 2, 256, dtype=bf, device=device)
-            vc = torch.empty_like(kc)
-            qo = torch.empty(T, 16, 256, dtype=bf, device=device)
-            return lambda: ops.qkv_rope_cache(qkv, 16, 2, w, w, pos, cos, sin, pos, kc, vc,
-                                              rotary_dim=64, weight_offset=1, q_out=qo)
-        out[key][str(T)] = timed(make, bytes_qkv_cache(T, 16, 2, 256, 64))
-    # gates
-    for name, d_, act, fp8 in (("glu_silu_bf16_d9728", INTER, ops.SILU, False),
-                               ("glu_gelu_bf16_d2048_fp8", 2048, ops.GELU_TANH, True),
-                               ("glu_gelu_bf16_d10240", 10240, ops.GELU_TANH, False)):
-        out[name] = {}
-        for T in (1, 64, 512, 4096):
-            gu0 = synth.glu_inputs(0, bf, T, d_)["gate_up"].to(device)
-
-            def make(gu0=gu0, T=T, d_=d_, act=act, fp8=fp8):
-                gu = gu0.clone()
-                o = torch.empty(T, d_, dtype=torch.uint8 if fp8 else bf, device=device)
-                return lambda: ops.glu_act(gu, act, out=o, fp8=fp8, inv_scale=40.0)
-            out[name][str(T)] = timed(make, bytes_glu(T, d_, out_s=1 if fp8 else 2))
+        for T in Ts:
+            nb = case_bytes(op, T, **kw)
+            us, cold = timed(lambda: probe_case(torch, ops, synth, op, bf, T, **kw), nb)
+            cus, _ = timed(lambda: probe_case(torch, ops, synth, "copy", bf, 1,
+                                              hidden=(nb + 31) // 32 * 32), nb)
+            gbs = nb / (us * 1e-6) / 1e9
+            tag = f"B{T // 16}" if op == "qk_dflash2" else str(T)
+            out[key][tag] = [round(us, 3), round(gbs, 1), round(gbs / peak, 4),
+                             "cold" if cold else "warm", round(cus, 3), round(cus / us, 3)]
     return out
+
+
+def sweep_summary(sw, t1):
+    """The key figures of the sweep in a few hundred bytes: per op, the
+    fraction of measured HBM peak and of the same-bytes copy at T = 256, 512
+    and the largest T; and the T = 1 microseconds per call."""
+    rows = {}
+    for key, by_t in sw.items():
+        ts = list(by_t)
+        pick = [t for t in ts if t in ("256", "512", "B16", "B64")] + [ts[-1]]
+        rows[key] = {t: [by_t[t][2], by_t[t][5]] for t in dict.fromkeys(pick)}
+    return {"format": "op -> T -> [fraction of measured HBM peak, fraction of the same-bytes "
+                      "copy's speed]; t1: median us per call, graph replay, warm L2",
+            "t1": {k: v["median"] for k, v in (t1 or {}).items() if "median" in v},
+            "ops": rows}
 
 
 def t1_latency(torch, ops, synth, device):
@@ -735,6 +824,8 @@ def t1_latency(torch, ops, synth, device):
 
 def main():
     args = parse()
+    if args.probe:
+        return run_probe(args)
     if args.impl == "reference":
         return run_reference(args)
 
@@ -912,15 +1003,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "decode seams of a 36-layer decoder: per layer add_rmsnorm, "
-                               "qk_norm_rope, add_rmsnorm, silu_and_mul",
-                   "T": T_DEC, "hidden": HID, "gate": INTER, "heads": [HQ, HK], "head_dim": HD,
-                   "rotary": [HD, "rotate_half"], "layers": LAYERS, "global_batch": T_DEC * world,
-                   "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB per step, "
-                         "distinct buffers per layer",
-                   "graph": "one CUDA graph per step (144 launches)",
-                   "pdl": os.environ.get("EDGE_OPS_PDL", "1") != "0",
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(world),
+        "launch": {"graph": "one CUDA graph per step (144 launches)",
+                   "pdl": os.environ.get("EDGE_OPS_PDL", "1") != "0"},
         "step_bytes": step_bytes,
         "roofline": roofline,
         "gpu_launches": launches_per_step * args.steps,
@@ -931,13 +1016,18 @@ def main():
         "clocks": clocks,
     }
     if world == 1:
+        t1 = None
         if not args.no_t1:
-            line["t1_us_per_call"] = t1_latency(torch, ops, synth, device)
+            t1 = line["t1_us_per_call"] = t1_latency(torch, ops, synth, device)
         if not args.no_sweep:
             line["sweep"] = sweep(torch, ops, synth, device, peak)
             line["sweep_format"] = ("T -> [us per call in back-to-back graph replay, GB/s, "
-                                    "fraction of measured HBM peak, L2 state]")
+                                    "fraction of measured HBM peak, L2 state, us of the copy "
+                                    "of the same bytes, copy us / op us]")
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        if not args.no_sweep:
+            # last, so that the end of the line carries the key figures
+            line["summary"] = sweep_summary(line["sweep"], t1)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -277,6 +277,18 @@ edge_status edge_rope(void* q_out, void* k_out, edge_dtype out_dt, const void* q
                       const int64_t* positions, const float* cos, const float* sin,
                       int64_t cache_len, float inv_scale, void* stream);
 
+/*
+ * Plain device copy of `bytes` bytes from src to dst, in the launch form of the
+ * operators above (a one-shot grid of 16-byte vectors, each CTA's source span
+ * prefetched into L2 before the dependent-launch wait).  It computes nothing:
+ * it is the yardstick the measurements set each operator against, the time a
+ * kernel of that form needs to move the same number of bytes.  No page defines
+ * it.  dst and src are device pointers of any alignment (16-byte aligned ones
+ * take the vector path); the ranges must not overlap (EDGE_ERR_ALIAS).
+ * bytes < 0: EDGE_ERR_SHAPE; bytes == 0 launches nothing.
+ */
+edge_status edge_copy(void* dst, const void* src, int64_t bytes, void* stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char* edge_status_str(edge_status status);
 

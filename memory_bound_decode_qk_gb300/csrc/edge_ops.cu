@@ -10,7 +10,6 @@
 #include <cstdint>
 #include <cstdlib>
 #include <atomic>
-#include <initializer_list>
 #include <mutex>
 
 #include "../../include/edge_ops.h"
@@ -67,55 +66,6 @@ bool pdl_enabled() {
         return !(v != nullptr && v[0] == '0');
     }();
     return on;
-}
-
-static int env_choice(const char* name, std::initializer_list<int> allowed) {
-    const char* v = std::getenv(name);
-    if (v == nullptr) return 0;
-    const int n = std::atoi(v);
-    for (int a : allowed) {
-        if (a == n) return n;
-    }
-    return 0;
-}
-
-int qk_path_override() {
-    static const int v = env_choice("EDGE_OPS_QK_PATH", {1, 3});
-    return v;
-}
-
-int rows_vt_override() {
-    static const int v = env_choice("EDGE_OPS_ROWS_VT", {1, 2, 4, 8});
-    return v;
-}
-
-int quad_threads_override() {
-    static const int v = env_choice("EDGE_OPS_QUAD_THREADS", {64, 128, 256});
-    return v;
-}
-
-int ln_warp_threads_override() {
-    static const int v = env_choice("EDGE_OPS_LN_WARP_THREADS", {32, 64, 128, 256});
-    return v;
-}
-
-int ln_warp_override() {
-    static const int v = [] {
-        const char* e = std::getenv("EDGE_OPS_LN_WARP");
-        if (e == nullptr || (e[0] != '0' && e[0] != '1') || e[1] != 0) return -1;
-        return e[0] - '0';
-    }();
-    return v;
-}
-
-int glu_unroll_override() {
-    static const int v = env_choice("EDGE_OPS_GLU_UNROLL", {1, 2, 4});
-    return v;
-}
-
-int quant_unroll_override() {
-    static const int v = env_choice("EDGE_OPS_QUANT_UNROLL", {1, 2, 4});
-    return v;
 }
 
 }  // namespace edge
@@ -538,6 +488,14 @@ edge_status edge_rope(void* q_out, void* k_out, edge_dtype out_dt, const void* q
     return qk_entry(q_out, k_out, out_dt, q, k, nullptr, nullptr, dt, tokens, q_heads, k_heads,
                     head_dim, rotary_dim, layout, positions, cos, sin, cache_len, 0.0f, 0,
                     inv_scale, 0 /* rotate only */, stream);
+}
+
+edge_status edge_copy(void* dst, const void* src, int64_t bytes, void* stream) {
+    if (dst == nullptr || src == nullptr) return EDGE_ERR_NULL;
+    if (bytes < 0) return EDGE_ERR_SHAPE;
+    if (overlap(span(dst, bytes), span(src, bytes))) return EDGE_ERR_ALIAS;
+    if (bytes == 0) return EDGE_OK;
+    return finish(edge::launch_copy(dst, src, bytes, static_cast<cudaStream_t>(stream)));
 }
 
 const char* edge_status_str(edge_status status) {

@@ -73,7 +73,8 @@ __device__ __forceinline__ float gate_fast(float g, float u) {
     }
     const float t = ex2_approx(__fmul_rn(-fabsf(v), kLog2e));
     const float num = v >= 0.0f ? 1.0f : t;
-    return __fmul_rn(__fmul_rn(g, u), __fmul_rn(num, rcp_approx_1to2(__fadd_rn(1.0f, t))));
+    // g * sigma(v) first, u last: g * u could overflow where sigma(v) = 0
+    return __fmul_rn(__fmul_rn(g, __fmul_rn(num, rcp_approx_1to2(__fadd_rn(1.0f, t)))), u);
 }
 
 // act(g) * u, accurate form (fp32 outputs).
@@ -86,26 +87,32 @@ __device__ __forceinline__ float gate_accurate(float g, float u) {
         ae = 0.0f;
         neg = g < 0.0f;
     } else {
-        // v = 2z = K g (1 + C g^2) in double-float arithmetic
-        const float g2 = __fmul_rn(g, g);
-        const float g2e = __fmaf_rn(g, g, -g2);
+        // v = 2z = K g (1 + C g^2) in double-float arithmetic.  Past |g| = 2^20,
+        // |v| > 2^56 and sigma(v) is exactly 0 or 1 in fp32, so g is clamped
+        // there: the double-float terms would overflow to inf - inf.
+        const float gc = fminf(fmaxf(g, -1048576.0f), 1048576.0f);
+        const float g2 = __fmul_rn(gc, gc);
+        const float g2e = __fmaf_rn(gc, gc, -g2);
         const float c = __fmul_rn(kC, g2);
         const float ce = __fmaf_rn(kC, g2, -c) + __fmaf_rn(kC, g2e, __fmul_rn(kClo, g2));
         const float s = __fadd_rn(1.0f, c);
         const float bb = __fsub_rn(s, 1.0f);
         const float se = __fadd_rn(__fadd_rn(__fsub_rn(1.0f, __fsub_rn(s, bb)), __fsub_rn(c, bb)), ce);
-        const float pq = __fmul_rn(g, s);
-        const float pe = __fmaf_rn(g, s, -pq) + __fmul_rn(g, se);
+        const float pq = __fmul_rn(gc, s);
+        const float pe = __fmaf_rn(gc, s, -pq) + __fmul_rn(gc, se);
         const float z = __fmul_rn(kK2, pq);
         const float ze = __fmaf_rn(kK2, pq, -z) + __fmaf_rn(kK2, pe, __fmul_rn(kK2lo, pq));
         neg = z < 0.0f;
         a = fabsf(z);
         ae = neg ? -ze : ze;
     }
-    // e^-(a + ae) = e^-a * e^-ae ~= e^-a (1 - ae), |ae| <= a few ulp of a
-    const float t = __fmul_rn(expf(-a), __fsub_rn(1.0f, ae));
+    // e^-(a + ae) = e^-a * e^-ae ~= e^-a (1 - ae), |ae| <= a few ulp of a.
+    // Wherever e^-a is nonzero (a < 104), |ae| < 2^-15; the clamp only keeps
+    // t = +0 past that, where a's ulp can exceed 1.
+    const float t = __fmul_rn(expf(-a), __fsub_rn(1.0f, fminf(fmaxf(ae, -0.25f), 0.25f)));
     const float num = neg ? t : 1.0f;
-    return __fmul_rn(__fmul_rn(g, u), __fdiv_rn(num, __fadd_rn(1.0f, t)));
+    // g * sigma first, u last (see gate_fast)
+    return __fmul_rn(__fmul_rn(g, __fdiv_rn(num, __fadd_rn(1.0f, t))), u);
 }
 
 template <typename T, bool FP8, int ACT>
@@ -240,18 +247,12 @@ cudaError_t launch_typed(const GluArgs& a, GluP& p, cudaStream_t s) {
         // one vector per thread and a one-shot grid (measured on GB300: 2 or 4
         // vectors per thread were slower at every size timed on its own,
         // 1.1x to 1.2x for the tanh-GELU gate with FP8 output)
-        int U = 1;
-        if (glu_unroll_override() > 0) U = glu_unroll_override();
-        int64_t blocks = ((int64_t)p.total + threads * U - 1) / (threads * U);
+        int64_t blocks = ((int64_t)p.total + threads - 1) / threads;
         const int64_t cap = (int64_t)sms * (2048 / threads) * 64;
         if (blocks > cap) blocks = cap;
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(threads);
-        switch (U) {
-            case 1: return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, 1>, p);
-            case 2: return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, 2>, p);
-            default: return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, 4>, p);
-        }
+        return cudaLaunchKernelEx(&cfg, glu_vec_kernel<T, FP8, ACT, 1>, p);
     }
     const int64_t total = a.rows * a.d;
     int64_t blocks = (total + 255) / 256;

@@ -89,6 +89,9 @@ struct QuantArgs {
 };
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
 
+// The yardstick copy (copy.cu): bytes from src to dst, validated.
+cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s);
+
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
@@ -102,25 +105,5 @@ int resident_ctas(const void* fn, int threads);
 // it is always safe as a dependent; it triggers its own dependents at its
 // start.
 bool pdl_enabled();
-
-// Launch-shape overrides for tuning (0: the built-in choice), read once from
-// EDGE_OPS_QK_PATH (1: one head per lane group, 3: four threads per head),
-// EDGE_OPS_ROWS_VT (target vectors per thread: 1, 2, 4 or 8),
-// EDGE_OPS_GLU_UNROLL and EDGE_OPS_QUANT_UNROLL (vectors per thread: 1, 2 or
-// 4).
-int qk_path_override();
-int rows_vt_override();
-int glu_unroll_override();
-int quant_unroll_override();
-// EDGE_OPS_LN_WARP: 1 one warp per LayerNorm row, 0 never; -1 (unset) the
-// built-in choice.
-int ln_warp_override();
-// EDGE_OPS_LN_WARP_THREADS: threads per CTA of the one-warp-per-row
-// LayerNorm (32, 64, 128 or 256); 0 (unset) the built-in choice.
-int ln_warp_threads_override();
-// EDGE_OPS_QUAD_THREADS: threads per CTA of the four-threads-per-head path
-// (64, 128 or 256); 0 (unset) the built-in choice.
-int quad_threads_override();
-
 
 }  // namespace edge

@@ -165,18 +165,13 @@ cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
         const int threads = 256;
         const int64_t per_block = (int64_t)(threads / 32) * hpw;
         int64_t blocks = ((int64_t)p.units + per_block - 1) / per_block;
-        int path = qk_path_override();
-        if (path == 0) {
-            // Measured on GB300 for every geometry: the one-shot grid wins
-            // up to a geometry's fraction of one wave of resident CTAs;
-            // past that, four threads per head (about 4x fewer instructions
-            // per head) win.
-            const int64_t hbytes = (int64_t)D * (int64_t)sizeof(T);
-            const double wave = (double)resident_ctas((const void*)vfn, threads) * sms *
-                                quad_min_waves((int)sizeof(T), a.layout, a.rotary_dim, hbytes);
-            path = (double)blocks > wave && quad_suits(a.layout, a.rotary_dim, hbytes) ? 3 : 1;
-        }
-        if (path == 3) {
+        // Measured on GB300 for every geometry: the one-shot grid wins up to a
+        // geometry's fraction of one wave of resident CTAs; past that, four
+        // threads per head (about 4x fewer instructions per head) win.
+        const int64_t hbytes = (int64_t)D * (int64_t)sizeof(T);
+        const double wave = (double)resident_ctas((const void*)vfn, threads) * sms *
+                            quad_min_waves((int)sizeof(T), a.layout, a.rotary_dim, hbytes);
+        if ((double)blocks > wave && quad_suits(a.layout, a.rotary_dim, hbytes)) {
             bool handled = false;
             cudaError_t e = launch_qk_quad<T, FP8>(a, p, cfg, &handled);
             if (handled || e != cudaSuccess) return e;

@@ -493,8 +493,7 @@ bool pipe_of(int C, int layout, int rq) {
 template <typename P, typename Fn>
 cudaError_t launch_quad(Fn fn, const P& arg, uint32_t units, bool pipe, int C,
                         cudaLaunchConfig_t cfg) {
-    int threads = C == 8 ? 64 : 128;
-    if (quad_threads_override() > 0) threads = quad_threads_override();
+    const int threads = C == 8 ? 64 : 128;
     const int64_t per_block = threads / K;
     int64_t blocks = ((int64_t)units + per_block - 1) / per_block;
     // the load-ahead form needs every CTA resident for all its passes

@@ -204,14 +204,8 @@ cudaError_t launch_typed(const QKVArgs& a, QKVP& k, cudaStream_t s, bool* handle
     int64_t blocks = ((int64_t)k.p.units + per_block - 1) / per_block;
     // the prologue's rule: the one-shot lane-group grid while it fits in one
     // wave of resident CTAs, four threads per head beyond
-    int path = qk_path_override();
-    if (path == 0) {
-        const int64_t wave = (int64_t)resident_ctas((const void*)vfn, threads) * sm_count();
-        path = blocks > wave && quad_suits(a.layout, k.p.rot, (int64_t)D * (int64_t)sizeof(T))
-                   ? 3
-                   : 1;
-    }
-    if (path == 3) {
+    const int64_t wave = (int64_t)resident_ctas((const void*)vfn, threads) * sm_count();
+    if (blocks > wave && quad_suits(a.layout, k.p.rot, (int64_t)D * (int64_t)sizeof(T))) {
         bool quad = false;
         cudaError_t e = launch_qkv_quad<T>(a, k, cfg, &quad);
         if (quad || e != cudaSuccess) return e;

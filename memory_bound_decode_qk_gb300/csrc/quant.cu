@@ -67,8 +67,7 @@ cudaError_t launch_typed(const QuantArgs& a, cudaStream_t s) {
     // four vectors per thread, all loaded before the first conversion
     // (measured on GB300: 1.18x over one vector at 2^23 elements, 1.35x at
     // 2^20; two vectors come within 2%)
-    int U = nvec > 0 ? 4 : 1;
-    if (quant_unroll_override() > 0 && nvec > 0) U = quant_unroll_override();
+    const int U = nvec > 0 ? 4 : 1;
     int64_t blocks = (work + threads * U - 1) / (threads * U);
     const int64_t cap = (int64_t)sm_count() * 64;
     if (blocks > cap) blocks = cap;
@@ -84,11 +83,8 @@ cudaError_t launch_typed(const QuantArgs& a, cudaStream_t s) {
     cfg.blockDim = dim3(threads);
     const char* xp = static_cast<const char*>(a.x);
     uint8_t* op = static_cast<uint8_t*>(a.out);
-    switch (U) {
-        case 2: return cudaLaunchKernelEx(&cfg, quant_kernel<T, 2>, xp, op, a.n, nvec, a.inv_scale);
-        case 4: return cudaLaunchKernelEx(&cfg, quant_kernel<T, 4>, xp, op, a.n, nvec, a.inv_scale);
-        default: return cudaLaunchKernelEx(&cfg, quant_kernel<T, 1>, xp, op, a.n, nvec, a.inv_scale);
-    }
+    if (U == 4) return cudaLaunchKernelEx(&cfg, quant_kernel<T, 4>, xp, op, a.n, nvec, a.inv_scale);
+    return cudaLaunchKernelEx(&cfg, quant_kernel<T, 1>, xp, op, a.n, nvec, a.inv_scale);
 }
 
 }  // namespace

@@ -11,14 +11,21 @@
 //
 // GB300 design.  Both ops move about 3 or 4 bytes of HBM traffic for every 2
 // flops.  A row is held in registers from its load to its store, so it makes
-// one HBM pass.  W warps own a row.  Each thread holds up to V 16-byte
-// vectors, and all of its loads are issued before any arithmetic, so a thread
-// keeps V (fused form: 2V) loads in flight.  The sum of squares is reduced
-// with warp shuffles, and through shared memory when W > 1.  W and V come
-// from the row length and the row count: few rows spread over more warps,
-// many rows favour more bytes in flight per thread.  Rows whose length or
-// alignment does not allow 16-byte vectors take a scalar two-pass kernel:
-// one CTA per row, and the second pass re-reads the row from L1/L2.
+// one HBM pass.  A CTA is a (32 W) x R block: threadIdx.y picks one of its R
+// rows and the W warps along x share that row, each thread holding up to V
+// 16-byte vectors.  Every load of a thread is issued before any arithmetic,
+// so it keeps V (fused form: 2V) loads in flight.  The grid is one-shot (one
+// CTA per R rows, no grid-stride loop), so between the dependent-launch wait
+// and the loads there is no index arithmetic beyond a multiply-add.  (Measured
+// on GB300: the earlier form, which divided the thread index by a run-time
+// row width and looped over rows, took 1.79 us per decode-width launch at
+// T = 64 and 3.1 us at T = 512 against 1.57 and 2.2 us for this one.)  The
+// sum of squares is reduced with warp shuffles, and through shared memory
+// with one barrier when W > 1.  W and V come from the row length and the row
+// count: few rows spread over more warps, many rows favour more bytes in
+// flight per thread.  Rows whose length or alignment does not allow 16-byte
+// vectors take a scalar two-pass kernel: one CTA per row, and the second pass
+// re-reads the row from L1/L2.
 #include "edge_common.cuh"
 #include "launch.h"
 
@@ -34,111 +41,113 @@ struct RowsP {
     int64_t rows;
     int hidden;
     int nvec;      // 16-byte vectors per row
-    int W;         // warps per row
-    int RPB;       // rows per CTA
     float eps, delta, inv, invH;  // invH = 1 / hidden (fp32)
 };
+
+// Sum of v over the W = blockDim.x / 32 warps that share this thread's row
+// (threadIdx.y): a shuffle tree per warp, then shared memory and one barrier.
+// Every thread of the CTA calls it.  A kernel that reduces twice passes two
+// buffers, so that no slot is rewritten before every reader has passed the
+// barrier that follows its first write.
+__device__ __forceinline__ float row_sum(float v, float* buf) {
+    v = group_sum<32>(v);
+    const int W = blockDim.x >> 5;
+    if (W > 1) {
+        const int wib = (threadIdx.y * blockDim.x + threadIdx.x) >> 5;
+        if ((threadIdx.x & 31) == 0) buf[wib] = v;
+        __syncthreads();
+        v = 0.0f;
+        for (int k = 0; k < W; ++k) v = __fadd_rn(v, buf[threadIdx.y * W + k]);
+    }
+    return v;
+}
 
 template <typename T, bool FP8, bool ADD, int V>
 __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
     constexpr int N = vec_elems<T>();
     __shared__ float red[16];
-    const int tpr = 32 * p.W;
-    const int g = threadIdx.x / tpr;
-    const int tid = threadIdx.x - g * tpr;
-    const int lane = threadIdx.x & 31;
-    const int wib = threadIdx.x >> 5;
-    const int64_t in_row = (int64_t)p.hidden * (int64_t)sizeof(T);
+    const int tid = threadIdx.x;
+    const int tpr = blockDim.x;
+    const int64_t row0 = (int64_t)blockIdx.x * blockDim.y;
+    const int64_t row = row0 + threadIdx.y;
+    const bool active = row < p.rows;
+    const int64_t in_row = (int64_t)p.nvec * 16;
     const int64_t out_row = FP8 ? (int64_t)p.hidden : in_row;
 
-    if (threadIdx.x == 0) {
-        // this CTA's first rows, and the weight (CTA 0), into L2 while the
-        // preceding grid drains
-        const int64_t r0 = (int64_t)blockIdx.x * p.RPB;
-        const int64_t r1 = r0 + p.RPB < p.rows ? r0 + p.RPB : p.rows;
-        prefetch_l2(p.x, r0 * in_row, r1 * in_row);
-        if (ADD) prefetch_l2(p.res, r0 * in_row, r1 * in_row);
-        if (blockIdx.x == 0) prefetch_l2(p.w, 0, in_row);
+    if (tid == 0 && threadIdx.y == 0) {
+        // this CTA's rows into L2 while the preceding grid drains
+        const int64_t r1 = row0 + blockDim.y < p.rows ? row0 + blockDim.y : p.rows;
+        prefetch_l2(p.x, row0 * in_row, r1 * in_row);
+        if (ADD) prefetch_l2(p.res, row0 * in_row, r1 * in_row);
     }
     pdl_wait();
     pdl_launch_dependents();
 
-    for (int64_t r0 = (int64_t)blockIdx.x * p.RPB; r0 < p.rows; r0 += (int64_t)gridDim.x * p.RPB) {
-        const int64_t row = r0 + g;
-        const bool active = row < p.rows;
-        const int64_t rsafe = active ? row : r0;
-        const uint4* xr = reinterpret_cast<const uint4*>(p.x + rsafe * in_row);
-        uint4* rr = ADD ? reinterpret_cast<uint4*>(p.res + rsafe * in_row) : nullptr;
+    const int64_t rsafe = active ? row : row0;
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + rsafe * in_row);
+    uint4* rr = ADD ? reinterpret_cast<uint4*>(p.res + rsafe * in_row) : nullptr;
 
-        // every load of the row (x, residual and the weight) is issued before
-        // any arithmetic: one memory round trip per row
-        const uint4* wv = reinterpret_cast<const uint4*>(p.w);
-        uint4 xv[V], rv[V], wr[V];
+    // every load of the row (x, residual and the weight) is issued before
+    // any arithmetic: one memory round trip per row
+    const uint4* wv = reinterpret_cast<const uint4*>(p.w);
+    uint4 xv[V], rv[V], wr[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
+    for (int i = 0; i < V; ++i) {
+        const int idx = tid + i * tpr;
+        const bool ok = active && idx < p.nvec;
+        xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (ADD) rv[i] = ok ? __ldcs(rr + idx) : make_uint4(0u, 0u, 0u, 0u);
+        wr[i] = (ok && wv != nullptr) ? __ldg(wv + idx) : make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    // beyond 32 terms per thread, two running sums alternating by vector
+    // (at most 4N sequential terms each, for the error bound of the
+    // tolerance)
+    constexpr bool kSplit = V * N > 32;
+    float ssp[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        float a[N];
+        unpack_vec<T, N>(xv[i], a);
+        if constexpr (ADD) {
+            // eager semantics: widen, add in fp32, round once to the dtype
+            float b[N];
+            unpack_vec<T, N>(rv[i], b);
+#pragma unroll
+            for (int e = 0; e < N; ++e) a[e] = round_to<T>(__fadd_rn(a[e], b[e]));
+            xv[i] = pack_vec<T, N>(a);
             const int idx = tid + i * tpr;
-            const bool ok = active && idx < p.nvec;
-            xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (ADD) rv[i] = ok ? __ldcs(rr + idx) : make_uint4(0u, 0u, 0u, 0u);
-            wr[i] = (ok && wv != nullptr) ? __ldg(wv + idx) : make_uint4(0u, 0u, 0u, 0u);
+            if (active && idx < p.nvec) rr[idx] = xv[i];
         }
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            ssp[kSplit ? (i & 1) : 0] = __fmaf_rn(a[e], a[e], ssp[kSplit ? (i & 1) : 0]);
+        }
+    }
+    const float ss = row_sum(kSplit ? __fadd_rn(ssp[0], ssp[1]) : ssp[0], red);
+    const float r = inv_rms(ss, p.invH, p.eps);
 
-        // beyond 32 terms per thread, two running sums alternating by vector
-        // (at most 4N sequential terms each, for the error bound of the
-        // tolerance)
-        constexpr bool kSplit = V * N > 32;
-        float ssp[2] = {0.0f, 0.0f};
+    char* orow = p.out + rsafe * out_row;
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            float a[N];
-            unpack_vec<T, N>(xv[i], a);
-            if constexpr (ADD) {
-                // eager semantics: widen, add in fp32, round once to the dtype
-                float b[N];
-                unpack_vec<T, N>(rv[i], b);
+    for (int i = 0; i < V; ++i) {
+        const int idx = tid + i * tpr;
+        if (!(active && idx < p.nvec)) continue;
+        float s[N], y[N];
+        unpack_vec<T, N>(xv[i], s);
+        if (wv != nullptr) {
+            float w[N];
+            unpack_vec<T, N>(wr[i], w);
 #pragma unroll
-                for (int e = 0; e < N; ++e) a[e] = round_to<T>(__fadd_rn(a[e], b[e]));
-                xv[i] = pack_vec<T, N>(a);
-                const int idx = tid + i * tpr;
-                if (active && idx < p.nvec) rr[idx] = xv[i];
-            }
+            for (int e = 0; e < N; ++e) y[e] = __fmul_rn(__fmul_rn(s[e], r), __fadd_rn(w[e], p.delta));
+        } else {
 #pragma unroll
-            for (int e = 0; e < N; ++e) {
-                ssp[kSplit ? (i & 1) : 0] = __fmaf_rn(a[e], a[e], ssp[kSplit ? (i & 1) : 0]);
-            }
+            for (int e = 0; e < N; ++e) y[e] = __fmul_rn(s[e], r);
         }
-        float ss = group_sum<32>(kSplit ? __fadd_rn(ssp[0], ssp[1]) : ssp[0]);
-        if (p.W > 1) {
-            if (lane == 0) red[wib] = ss;
-            __syncthreads();
-            ss = 0.0f;
-            for (int k = 0; k < p.W; ++k) ss = __fadd_rn(ss, red[g * p.W + k]);
-            __syncthreads();
-        }
-        const float r = inv_rms(ss, p.invH, p.eps);
-
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const int idx = tid + i * tpr;
-            if (!(active && idx < p.nvec)) continue;
-            float s[N], y[N];
-            unpack_vec<T, N>(xv[i], s);
-            if (wv != nullptr) {
-                float w[N];
-                unpack_vec<T, N>(wr[i], w);
-#pragma unroll
-                for (int e = 0; e < N; ++e) y[e] = __fmul_rn(__fmul_rn(s[e], r), __fadd_rn(w[e], p.delta));
-            } else {
-#pragma unroll
-                for (int e = 0; e < N; ++e) y[e] = __fmul_rn(s[e], r);
-            }
-            char* orow = p.out + row * out_row;
-            if constexpr (FP8) {
-                auto q8 = quantize_vec<N>(y, p.inv);
-                reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
-            } else {
-                reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
-            }
+        if constexpr (FP8) {
+            auto q8 = quantize_vec<N>(y, p.inv);
+            reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
+        } else {
+            reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
         }
     }
 }
@@ -189,23 +198,6 @@ __global__ void __launch_bounds__(256) rows_generic_kernel(RowsP p) {
     }
 }
 
-// Sum of v over the W warps that own a row: one shuffle tree per warp, then
-// shared memory, with one barrier.  Every thread of the CTA calls it the same
-// number of times.  The partial sums go to `buf`, which the caller alternates
-// between two reductions, so a buffer is rewritten only after a later barrier
-// that every reader of its previous contents has passed.
-__device__ __forceinline__ float row_sum_alt(float v, const RowsP& p, int g, int lane, int wib,
-                                             float* buf) {
-    v = group_sum<32>(v);
-    if (p.W > 1) {
-        if (lane == 0) buf[wib] = v;
-        __syncthreads();
-        v = 0.0f;
-        for (int k = 0; k < p.W; ++k) v = __fadd_rn(v, buf[g * p.W + k]);
-    }
-    return v;
-}
-
 // One-read LayerNorm (FlashRT siglip_layernorm_1read): the row stays in
 // registers for the mean, the variance of the centred values and the
 // output, so x is read from HBM once.  y = (x - mu) r gamma + beta.  gamma
@@ -215,99 +207,91 @@ template <typename T, bool FP8, int V>
 __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
     constexpr int N = vec_elems<T>();
     __shared__ float red_mu[16], red_var[16];
-    const int tpr = 32 * p.W;
-    const int g = threadIdx.x / tpr;
-    const int tid = threadIdx.x - g * tpr;
-    const int lane = threadIdx.x & 31;
-    const int wib = threadIdx.x >> 5;
-    const int64_t in_row = (int64_t)p.hidden * (int64_t)sizeof(T);
+    const int tid = threadIdx.x;
+    const int tpr = blockDim.x;
+    const int64_t row0 = (int64_t)blockIdx.x * blockDim.y;
+    const int64_t row = row0 + threadIdx.y;
+    const bool active = row < p.rows;
+    const int64_t in_row = (int64_t)p.nvec * 16;
     const int64_t out_row = FP8 ? (int64_t)p.hidden : in_row;
     const uint4* gv = reinterpret_cast<const uint4*>(p.w);
     const uint4* bv = reinterpret_cast<const uint4*>(p.beta);
 
-    if (threadIdx.x == 0) {
-        const int64_t r0 = (int64_t)blockIdx.x * p.RPB;
-        const int64_t r1 = r0 + p.RPB < p.rows ? r0 + p.RPB : p.rows;
-        prefetch_l2(p.x, r0 * in_row, r1 * in_row);
-        if (blockIdx.x == 0) {
-            prefetch_l2(p.w, 0, in_row);
-            prefetch_l2(p.beta, 0, in_row);
-        }
+    if (tid == 0 && threadIdx.y == 0) {
+        const int64_t r1 = row0 + blockDim.y < p.rows ? row0 + blockDim.y : p.rows;
+        prefetch_l2(p.x, row0 * in_row, r1 * in_row);
     }
     pdl_wait();
     pdl_launch_dependents();
 
-    for (int64_t r0 = (int64_t)blockIdx.x * p.RPB; r0 < p.rows; r0 += (int64_t)gridDim.x * p.RPB) {
-        const int64_t row = r0 + g;
-        const bool active = row < p.rows;
-        const uint4* xr = reinterpret_cast<const uint4*>(p.x + (active ? row : r0) * in_row);
-        uint4 xv[V];
+    const int64_t rsafe = active ? row : row0;
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + rsafe * in_row);
+    uint4 xv[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const int idx = tid + i * tpr;
-            const bool ok = active && idx < p.nvec;
-            xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < V; ++i) {
+        const int idx = tid + i * tpr;
+        const bool ok = active && idx < p.nvec;
+        xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // beyond 32 terms per thread, two running sums alternating by vector
+    constexpr bool kSplit = V * N > 32;
+    float sp[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        float a[N];
+        unpack_vec<T, N>(xv[i], a);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            sp[kSplit ? (i & 1) : 0] = __fadd_rn(sp[kSplit ? (i & 1) : 0], a[e]);
         }
-        // beyond 32 terms per thread, two running sums alternating by vector
-        constexpr bool kSplit = V * N > 32;
-        float sp[2] = {0.0f, 0.0f};
+    }
+    const float sum = kSplit ? __fadd_rn(sp[0], sp[1]) : sp[0];
+    const float mu = __fmul_rn(row_sum(sum, red_mu), p.invH);
+    float sqp[2] = {0.0f, 0.0f};
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            float a[N];
-            unpack_vec<T, N>(xv[i], a);
+    for (int i = 0; i < V; ++i) {
+        const int idx = tid + i * tpr;
+        if (!(active && idx < p.nvec)) continue;  // padding lanes add nothing
+        float a[N];
+        unpack_vec<T, N>(xv[i], a);
 #pragma unroll
-            for (int e = 0; e < N; ++e) {
-                sp[kSplit ? (i & 1) : 0] = __fadd_rn(sp[kSplit ? (i & 1) : 0], a[e]);
-            }
+        for (int e = 0; e < N; ++e) {
+            const float d = __fsub_rn(a[e], mu);
+            sqp[kSplit ? (i & 1) : 0] = __fmaf_rn(d, d, sqp[kSplit ? (i & 1) : 0]);
         }
-        const float sum = kSplit ? __fadd_rn(sp[0], sp[1]) : sp[0];
-        const float mu = __fmul_rn(row_sum_alt(sum, p, g, lane, wib, red_mu), p.invH);
-        float sqp[2] = {0.0f, 0.0f};
+    }
+    const float sq = kSplit ? __fadd_rn(sqp[0], sqp[1]) : sqp[0];
+    const float r = inv_rms(row_sum(sq, red_var), p.invH, p.eps);
+    // gamma and beta (L1/L2-resident), all issued before the output loop
+    uint4 gr[V], br[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const int idx = tid + i * tpr;
-            if (!(active && idx < p.nvec)) continue;  // padding lanes add nothing
-            float a[N];
-            unpack_vec<T, N>(xv[i], a);
+    for (int i = 0; i < V; ++i) {
+        const int idx = tid + i * tpr;
+        const bool ok = active && idx < p.nvec;
+        gr[i] = (ok && gv != nullptr) ? __ldg(gv + idx) : make_uint4(0u, 0u, 0u, 0u);
+        br[i] = (ok && bv != nullptr) ? __ldg(bv + idx) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    char* orow = p.out + rsafe * out_row;
 #pragma unroll
-            for (int e = 0; e < N; ++e) {
-                const float d = __fsub_rn(a[e], mu);
-                sqp[kSplit ? (i & 1) : 0] = __fmaf_rn(d, d, sqp[kSplit ? (i & 1) : 0]);
-            }
+    for (int i = 0; i < V; ++i) {
+        const int idx = tid + i * tpr;
+        if (!(active && idx < p.nvec)) continue;
+        float a[N], gg[N], bb[N], y[N];
+        unpack_vec<T, N>(xv[i], a);
+        if (gv != nullptr) unpack_vec<T, N>(gr[i], gg);
+        if (bv != nullptr) unpack_vec<T, N>(br[i], bb);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            float v = __fmul_rn(__fsub_rn(a[e], mu), r);
+            if (gv != nullptr) v = __fmul_rn(v, gg[e]);
+            if (bv != nullptr) v = __fadd_rn(v, bb[e]);
+            y[e] = v;
         }
-        const float sq = kSplit ? __fadd_rn(sqp[0], sqp[1]) : sqp[0];
-        const float r = inv_rms(row_sum_alt(sq, p, g, lane, wib, red_var), p.invH, p.eps);
-        // gamma and beta (L1/L2-resident), all issued before the output loop
-        uint4 gr[V], br[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const int idx = tid + i * tpr;
-            const bool ok = active && idx < p.nvec;
-            gr[i] = (ok && gv != nullptr) ? __ldg(gv + idx) : make_uint4(0u, 0u, 0u, 0u);
-            br[i] = (ok && bv != nullptr) ? __ldg(bv + idx) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const int idx = tid + i * tpr;
-            if (!(active && idx < p.nvec)) continue;
-            float a[N], gg[N], bb[N], y[N];
-            unpack_vec<T, N>(xv[i], a);
-            if (gv != nullptr) unpack_vec<T, N>(gr[i], gg);
-            if (bv != nullptr) unpack_vec<T, N>(br[i], bb);
-#pragma unroll
-            for (int e = 0; e < N; ++e) {
-                float v = __fmul_rn(__fsub_rn(a[e], mu), r);
-                if (gv != nullptr) v = __fmul_rn(v, gg[e]);
-                if (bv != nullptr) v = __fadd_rn(v, bb[e]);
-                y[e] = v;
-            }
-            char* orow = p.out + row * out_row;
-            if constexpr (FP8) {
-                auto q8 = quantize_vec<N>(y, p.inv);
-                reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
-            } else {
-                reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
-            }
+        if constexpr (FP8) {
+            auto q8 = quantize_vec<N>(y, p.inv);
+            reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
+        } else {
+            reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
         }
     }
 }
@@ -481,10 +465,19 @@ __global__ void __launch_bounds__(256) ln_generic_kernel(RowsP p) {
     }
 }
 
-// Launch shape of the vector kernels: W warps per row, V vectors per thread,
-// RPB rows per CTA.  false when the row needs the generic kernel.
+// Launch shape of the vector kernels.
+struct VecShape {
+    int nvec;  // 16-byte vectors per row
+    int W;     // warps per row (blockDim.x = 32 W)
+    int R;     // rows per CTA (blockDim.y)
+    int V;     // vectors per thread (template argument)
+};
+
+// The vector shape of a call, or false when the row needs the generic kernel
+// (length or alignment not a multiple of 16 bytes, more than 16 x 32 x 8
+// vectors per row, or more CTAs than a one-shot grid holds).
 template <typename T, bool FP8>
-bool vec_shape(const RowsArgs& a, int sms, RowsP& p, int& V) {
+bool vec_shape(const RowsArgs& a, int sms, VecShape& v) {
     constexpr int N = vec_elems<T>();
     auto aligned = [](const void* ptr, uintptr_t n) {
         return ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) % n) == 0;
@@ -500,22 +493,14 @@ bool vec_shape(const RowsArgs& a, int sms, RowsP& p, int& V) {
     // one input stream per row (plain RMSNorm): more vectors per thread keep
     // enough bytes in flight once there are many rows (measured on GB300)
     if (!a.residual && !a.layernorm && a.rows >= 8 * sms) vt = 4;
-    // at most 8 warps per row: wider rows take two vectors per thread, which
-    // halves the CTA and the cross-warp combine (measured on GB300: the
-    // decode step at hidden 2560 and T = 64 4% faster, its row launches alone
-    // within 2%, and hidden 4096 at T = 64 6% faster)
-    if (vt == 1 && nvec > 8 * 32) vt = 2;
-    if (rows_vt_override() > 0) vt = rows_vt_override();
     int W = (int)((nvec + 32 * vt - 1) / (32 * vt));
     if (W > 16) W = 16;
     const int64_t per = (nvec + 32 * W - 1) / (32 * W);
-    V = per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
-    int RPB = 256 / (32 * W);
-    if (RPB < 1) RPB = 1;
-    p.nvec = (int)nvec;
-    p.W = W;
-    p.RPB = RPB;
-    return true;
+    v.V = per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
+    v.W = W;
+    v.R = 256 / (32 * W) > 1 ? 256 / (32 * W) : 1;
+    v.nvec = (int)nvec;
+    return (a.rows + v.R - 1) / v.R <= (int64_t)INT32_MAX;
 }
 
 template <typename T, bool FP8, bool ADD>
@@ -529,28 +514,26 @@ cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
 
-    int V = 1;
-    int ln_warp = ln_warp_override();
-    if (ln_warp < 0) {
-        // one warp per row once there are many rows.  Measured crossover on
-        // GB300: T = 768 at width 1152 (5 vectors per lane), T = 1536 at
-        // width 2048 (8 vectors per lane, fewer CTAs per SM)
-        const int64_t lanes_vecs = ((int64_t)a.hidden / vec_elems<T>() + 31) / 32;
-        ln_warp = a.rows >= (lanes_vecs <= 5 ? 5 : 10) * (int64_t)sms;
-    }
-    if (vec_shape<T, FP8>(a, sms, p, V) && a.layernorm && p.nvec <= 256 && ln_warp) {
+    VecShape v;
+    const bool vec = vec_shape<T, FP8>(a, sms, v);
+    if (vec) p.nvec = v.nvec;
+    // LayerNorm: one warp per row once there are many rows.  Measured
+    // crossover on GB300: T = 768 at width 1152 (5 vectors per lane), T = 1536
+    // at width 2048 (8 vectors per lane, fewer CTAs per SM)
+    const int64_t lanes_vecs = ((int64_t)a.hidden / vec_elems<T>() + 31) / 32;
+    const bool ln_warp = a.rows >= (lanes_vecs <= 5 ? 5 : 10) * (int64_t)sms;
+    if (vec && a.layernorm && v.nvec <= 256 && ln_warp) {
         // 4 rows per CTA: finer CTAs balance the last wave (measured on
         // GB300: 1.35x faster than 8 rows per CTA at T = 4096, width 1152)
-        int threads = 128;
-        if (ln_warp_threads_override() > 0) threads = ln_warp_threads_override();
+        const int threads = 128;
         const int64_t rpb = threads / 32;
         int64_t blocks = (a.rows + rpb - 1) / rpb;
         const int64_t cap = (int64_t)sms * 64;
         if (blocks > cap) blocks = cap;
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(threads);
-        cfg.dynamicSmemBytes = (size_t)2 * p.nvec * 16;
-        switch ((p.nvec + 31) / 32) {
+        cfg.dynamicSmemBytes = (size_t)2 * v.nvec * 16;
+        switch ((v.nvec + 31) / 32) {
             case 1: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 1>, p);
             case 2: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 2>, p);
             case 3: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 3>, p);
@@ -561,22 +544,19 @@ cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
             default: return cudaLaunchKernelEx(&cfg, ln_warp_kernel<T, FP8, 8>, p);
         }
     }
-    if (vec_shape<T, FP8>(a, sms, p, V)) {
-        const int threads = 32 * p.W * p.RPB;
-        int64_t blocks = (a.rows + p.RPB - 1) / p.RPB;
-        const int64_t cap = (int64_t)sms * (2048 / threads) * 8;
-        if (blocks > cap) blocks = cap;
-        cfg.gridDim = dim3((unsigned)blocks);
-        cfg.blockDim = dim3(threads);
+    if (vec) {
+        // one-shot grid: one CTA per R rows
+        cfg.gridDim = dim3((unsigned)((a.rows + v.R - 1) / v.R));
+        cfg.blockDim = dim3(32 * v.W, v.R);
         if (a.layernorm) {
-            switch (V) {
+            switch (v.V) {
                 case 1: return cudaLaunchKernelEx(&cfg, ln_vec_kernel<T, FP8, 1>, p);
                 case 2: return cudaLaunchKernelEx(&cfg, ln_vec_kernel<T, FP8, 2>, p);
                 case 4: return cudaLaunchKernelEx(&cfg, ln_vec_kernel<T, FP8, 4>, p);
                 default: return cudaLaunchKernelEx(&cfg, ln_vec_kernel<T, FP8, 8>, p);
             }
         }
-        switch (V) {
+        switch (v.V) {
             case 1: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 1>, p);
             case 2: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 2>, p);
             case 4: return cudaLaunchKernelEx(&cfg, rows_vec_kernel<T, FP8, ADD, 4>, p);
@@ -613,8 +593,6 @@ cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s) {
     p.rows = a.rows;
     p.hidden = (int)a.hidden;
     p.nvec = 0;
-    p.W = 1;
-    p.RPB = 1;
     p.eps = a.eps;
     p.delta = (float)a.weight_offset;
     p.inv = a.inv_scale;

@@ -26,7 +26,7 @@ STATUS = {
 }
 EXPORTS = ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope",
            "edge_qk_norm_rope_ex", "edge_rope", "edge_layernorm", "edge_quantize_fp8",
-           "edge_qkv_rope_cache",
+           "edge_qkv_rope_cache", "edge_copy",
            "edge_status_str", "edge_last_cuda_error", "edge_version")
 QK_ROTATE_UNROUNDED = 1
 
@@ -75,9 +75,10 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
     L.edge_quantize_fp8.argtypes = [P, P, I, I64, F, P]
     L.edge_qkv_rope_cache.argtypes = [P, P, P, P, P, P, I, I64, I32, I32, I32, I32, I, P, P, P,
                                       I64, P, I64, F, I, I, P]
+    L.edge_copy.argtypes = [P, P, I64, P]
     for name in ("edge_rmsnorm", "edge_add_rmsnorm", "edge_glu_act", "edge_qk_norm_rope",
                  "edge_qk_norm_rope_ex", "edge_rope", "edge_layernorm", "edge_quantize_fp8",
-                 "edge_qkv_rope_cache"):
+                 "edge_qkv_rope_cache", "edge_copy"):
         getattr(L, name).restype = I
     L.edge_status_str.argtypes = [I]
     L.edge_status_str.restype = ctypes.c_char_p
@@ -170,6 +171,19 @@ def layernorm(x, gamma=None, beta=None, *, eps=1e-6, out=None, fp8=False, inv_sc
     dt = _dt(x)
     _check(lib().edge_layernorm(_ptr(out), _out_dt(fp8, dt), _ptr(x), _ptr(gamma), _ptr(beta), dt,
                                 rows, hidden, eps, inv_scale, _stream(stream)), "edge_layernorm")
+    return out
+
+
+def copy(src, *, out=None, stream=None):
+    """The yardstick copy: src's bytes into out (a new tensor like src when
+    None), in the operators' launch form.  Returns out."""
+    _need_contig(src, out)
+    if out is None:
+        out = torch.empty_like(src)
+    nbytes = src.numel() * src.element_size()
+    if out.numel() * out.element_size() != nbytes:
+        raise ValueError("copy: out must hold as many bytes as src")
+    _check(lib().edge_copy(_ptr(out), _ptr(src), nbytes, _stream(stream)), "edge_copy")
     return out
 
 

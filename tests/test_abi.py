@@ -95,6 +95,7 @@ def test_zero_rows_is_ok_and_launches_nothing(L):
     assert add(L, rows=0) == OK
     assert glu(L, rows=0) == OK
     assert qk(L, T=0) == OK
+    assert L.edge_copy(O, X, 0, None) == OK
     # no CUDA call was made: no sticky error recorded
     assert L.edge_last_cuda_error() == 0
 
@@ -158,6 +159,11 @@ def test_zero_rows_is_ok_and_launches_nothing(L):
                                      POS, COS, SIN, 4096, POS + 4096, 16, 1e-6, 0, 2, None), VALUE),
     (lambda L: L.edge_qkv_rope_cache(QO, KO, KO + 65536, Q, WQ, WK, FP8, 4, 8, 2, 128, 64, 0,
                                      POS, COS, SIN, 4096, POS + 4096, 16, 1e-6, 0, 1, None), DTYPE),
+    (lambda L: L.edge_copy(None, X, 16, None), NULL),
+    (lambda L: L.edge_copy(O, None, 16, None), NULL),
+    (lambda L: L.edge_copy(O, X, -1, None), SHAPE),
+    (lambda L: L.edge_copy(X + 8, X, 16, None), ALIAS),
+    (lambda L: L.edge_copy(X, X + 15, 16, None), ALIAS),
     (lambda L: rms(L, hidden=2 ** 25, rows=1), UNSUP),
     # one past each declared limit: rows of 2**24, heads of 2048, 2**31 - 1 units
     (lambda L: rms(L, hidden=2 ** 24 + 8, rows=1), UNSUP),

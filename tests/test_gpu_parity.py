@@ -14,6 +14,8 @@ Bands: tests/tolerances.py, which gives the fp32 error analysis behind each
 (ETA_NORM for every normalized output, a per-element band for the gates),
 pinned on the CPU by tests/test_tolerances.py.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -313,20 +315,32 @@ def test_qk_without_cache_rows_rotates_nothing(T):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-@pytest.mark.parametrize("op", ["qk", "qkv"])
-def test_positions_rewritten_by_the_preceding_kernel(op):
+# Geometries of the lane-group prologue under a position rewrite: one head per
+# warp (bf16, 256), two heads per warp (bf16, 128), fp32 heads (one per warp,
+# four channels per lane) and the interleaved cache load.
+REWRITE_GEOMS = {
+    "bf16_d256_rot64": (torch.bfloat16, 16, 2, 256, 64, 0),
+    "bf16_d128_rot128": (torch.bfloat16, 8, 2, 128, 128, 0),
+    "f32_d128_rot64": (torch.float32, 4, 2, 128, 64, 0),
+    "bf16_d256_interleaved": (torch.bfloat16, 8, 2, 256, 256, 1),
+}
+
+
+@pytest.mark.parametrize("op,geom", [("qk", g) for g in REWRITE_GEOMS] + [("qkv", "bf16_d256_rot64")])
+def test_positions_rewritten_by_the_preceding_kernel(op, geom):
     # The prologue's lane-group kernels read each token's position before
     # their dependent-launch wait, as an address hint only, and check it
     # after the wait.  Here the kernel just before them on the stream (a
     # residual add whose residual is the positions array) rewrites the
     # positions while the prologue may already be resident: a stale hint
     # must cost a reload, never a wrong row.
-    T, Hq, Hk, D, rot, P = 12, 16, 2, 256, 64, 200
+    dtype, Hq, Hk, D, rot, layout = REWRITE_GEOMS[geom]
+    T, P = 12, 200
     old = np.array([5, 6, 7, 250, 9, 10, 11, 12, 13, 14, 15, 16], np.int64)
     new = np.array([7, 6, 201, 3, 100, 10, 0, 199, 13, 255, 1, 2], np.int64)
-    inp = synth.qk_inputs(0, torch.bfloat16, T, Hq, Hk, D, rot, theta=1e7, cache_len=P,
+    inp = synth.qk_inputs(0, dtype, T, Hq, Hk, D, rot, theta=1e7, cache_len=P,
                           positions=new, w_std=0.05)
-    fmt = oracle.BF16
+    fmt = TORCH_FMT[dtype]
     pos = dev(torch.from_numpy(old))
     cs, sn = dev(inp["cos"]), dev(inp["sin"])
     wq, wk = dev(inp["wq"]), dev(inp["wk"])
@@ -334,13 +348,13 @@ def test_positions_rewritten_by_the_preceding_kernel(op):
     scratch = torch.empty_like(delta)
     if op == "qk":
         ref = oracle.qk_norm_rope(storage(inp["q"]), storage(inp["k"]), storage(inp["wq"]),
-                                  storage(inp["wk"]), fmt, rot, oracle.ROTATE_HALF, new,
+                                  storage(inp["wk"]), fmt, rot, layout, new,
                                   storage(inp["cos"]), storage(inp["sin"]), 1e-6, 1, eta=ETA_NORM)
         q, k = dev(inp["q"]), dev(inp["k"])
         qo, ko = torch.empty_like(q), torch.empty_like(k)
         edge_ops.add_rmsnorm(delta, pos.view(torch.bfloat16).view(1, -1), None, out=scratch)
-        edge_ops.qk_norm_rope(q, k, wq, wk, pos, cs, sn, rotary_dim=rot, weight_offset=1,
-                              q_out=qo, k_out=ko)
+        edge_ops.qk_norm_rope(q, k, wq, wk, pos, cs, sn, rotary_dim=rot, layout=layout,
+                              weight_offset=1, q_out=qo, k_out=ko)
         torch.cuda.synchronize()
         assert np.array_equal(pos.cpu().numpy(), new)
         check_out("q", storage(qo.cpu()), ref.q_out, ref.q_pre, ref.q_mag, fmt, fmt, ETA_NORM,
@@ -533,6 +547,50 @@ def run_glu(c, act, fp8=False, seed=0):
 @pytest.mark.parametrize("act", [oracle.SILU, oracle.GELU_TANH])
 def test_glu(name, act):
     run_glu(GLU_CASES[name], act)
+
+
+# (g, u) pairs at the edges of each dtype's range.  Where the logistic argument
+# v is past 200 (sigma exactly 0 or 1 in fp32) or the exact result underflows
+# to zero, the output must match the oracle bit for bit (signed zeros
+# included); the others take the gate band.  (-3e38, 3e38) and (-1e20, 1e20)
+# would give inf * 0 = NaN if g * u were formed before sigma.  e^-|v| stays an
+# fp32 normal wherever a result is representable and nonzero.
+GLU_EXTREMES = {
+    torch.bfloat16: [(-1e20, 1e20), (1e20, 1e18), (-1e20, -1e20), (1e20, -1e18), (-3e38, 1.0),
+                     (-3e38, 3e38), (3e38, 1.0), (0.0, 3e38), (-0.0, 5.0), (-60.0, 1e30),
+                     (-80.0, 1e35), (100.0, 1e30), (-1e5, 1e33), (1e-30, 1e-30), (-200.0, 3.0),
+                     (-3.0, 1e30)],
+    torch.float16: [(-6e4, 6e4), (6e4, 1.0), (-6e4, -6e4), (-20.0, 6e4), (-9.0, 6e4), (0.0, 6e4),
+                    (-0.0, 5.0), (100.0, 600.0), (-1e4, 6e4), (1e-7, 1e-7), (15.0, 4000.0),
+                    (-15.0, 4000.0), (-60.0, 6e4), (-3.0, 6e4), (30.0, -2000.0), (-30.0, 2000.0)],
+}
+GLU_EXTREMES[torch.float32] = GLU_EXTREMES[torch.bfloat16]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("act", [oracle.SILU, oracle.GELU_TANH])
+@pytest.mark.parametrize("extra", [0, 1])
+def test_glu_extremes(dtype, act, extra):
+    # extra = 1 adds a seventeenth pair, which takes the scalar kernel
+    pairs = GLU_EXTREMES[dtype] + [(1.0, 1.0)] * extra
+    d = len(pairs)
+    g = torch.tensor([p[0] for p in pairs], dtype=torch.float64)
+    u = torch.tensor([p[1] for p in pairs], dtype=torch.float64)
+    gu = torch.cat([g, u]).to(dtype).view(1, 2 * d)
+    fmt = TORCH_FMT[dtype]
+    ref, pre = oracle.glu_act(storage(gu), fmt, act)
+    out = Guarded((1, d), dtype)
+    edge_ops.glu_act(gu.cuda(), act, out=out.t)
+    torch.cuda.synchronize()
+    out.check()
+    got = storage(out.t.cpu())
+    gv = oracle.decode(storage(gu), fmt)[:, :d]
+    v = gv if act == oracle.SILU else \
+        2.0 * math.sqrt(2.0 / math.pi) * (gv + 0.044715 * gv ** 3)
+    exact = (np.abs(v) >= 200.0) | (oracle.decode(ref, fmt) == 0.0)
+    assert np.array_equal(got[exact], ref[exact]), report("glu extremes (exact)", got == ref)
+    check_out("glu extremes", got[~exact], ref[~exact], pre[~exact], np.abs(pre[~exact]), fmt,
+              fmt, gate_eta(gv[~exact], act))
 
 
 FP8_GLU = {
@@ -952,3 +1010,20 @@ def test_qk_at_the_largest_head(c):
 def test_qkv_at_the_largest_head():
     run_qkv(dict(dtype=torch.bfloat16, T=3, Hq=2, Hk=1, D=2048, rot=1024, layout=0, norm=True,
                  offset=1, S=4))
+
+
+# ---------------------------------------------------------------- yardstick copy
+
+@pytest.mark.parametrize("nbytes,dst_off,src_off", [
+    (16, 0, 0), (4096, 0, 0), (4096 + 7, 0, 0), ((1 << 20) + 48, 0, 0), ((1 << 22) + 5, 0, 0),
+    (3001, 1, 3), (65536 + 9, 8, 8), (1, 0, 0)])
+def test_copy_is_exact(nbytes, dst_off, src_off):
+    # the measurements' yardstick: every byte copied, nothing written outside
+    g = torch.Generator().manual_seed(nbytes)
+    src_raw = torch.randint(0, 256, (nbytes + 32,), generator=g, dtype=torch.uint8).cuda()
+    src = src_raw[src_off:src_off + nbytes]
+    out = Guarded((nbytes,), torch.uint8, dst_off)
+    edge_ops.copy(src, out=out.t)
+    torch.cuda.synchronize()
+    out.check()
+    assert torch.equal(out.t.cpu(), src.cpu())

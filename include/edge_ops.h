@@ -151,10 +151,8 @@ edge_status edge_glu_act(void* out, edge_dtype out_dt, const void* gate_up, edge
  *        a' = a c - b s,   b' = b c + a s   (fp32, then one rounding)
  *   Channels at or past rotary_dim carry m.  A token whose position is
  *   negative or >= cache_len is normalized but not rotated, and no cache row
- *   at that position is read (R5), so no device synchronization is needed.
- *   (Every cache read lies inside [0, cache_len): a row loaded at a position
- *   read before the dependent-launch wait is used only if the position read
- *   after it agrees.)
+ *   at that position is read (R5), so no device synchronization is needed:
+ *   every cache read lies inside [0, cache_len).
  *
  * q, k:        [tokens, q_heads, head_dim] and [tokens, k_heads, head_dim]
  *              of dt.  This is the innermost-first [head_dim, heads, tokens]

@@ -172,9 +172,8 @@ __device__ __forceinline__ float inv_rms(float ss, float inv_n, float eps) {
 // kernel was launched with programmatic stream serialization.  wait() blocks
 // until the preceding grid in the stream has completed and its writes are
 // visible, so every kernel calls it before its first global load whose value
-// it uses.  Before it, a kernel only prefetches into L2 and, in the
-// prologue's lane-group kernels, reads a position at L2 as an address hint
-// that is checked against the same position read after the wait.
+// it uses.  Before it, a kernel only computes addresses and prefetches into
+// L2.
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }

@@ -16,9 +16,8 @@
 //   - The rotate-half partner vector sits half/N lanes away and comes over a
 //     shuffle.  Interleaved pairs sit inside one vector.
 //   - cos/sin entries are read from L1: every head of a token shares the row.
-//   - The row is loaded at a position hint read before the dependent-launch
-//     wait, next to the position itself, and reloaded only if they differ:
-//     one round trip for the position and its row.
+//   - The grid is one-shot: one unit per lane group, its address computed
+//     before the dependent-launch wait.
 // Units are ordered token-major, so the warps of a CTA share cos/sin rows and
 // the norm weights.  Streamed inputs use evict-first loads.
 // Many heads: the four-threads-per-head path (qk_quad.cu) takes over past a
@@ -33,58 +32,46 @@ namespace {
 
 // ---------------------------------------------------------------- decode-width path
 
-// One head per lane group, a one-shot grid.  Every load of a head (data,
-// weight, position) is issued up front; the cache row follows the position.
+// One head per lane group, a one-shot grid: every unit of the grid is one
+// head, so the unit's addresses are known before the dependent-launch wait.
+// Every load of a head (data, weight, position) is issued right after it; the
+// cache row follows the position, an L1/L2 hit for every head of a token but
+// the first.  (Measured on GB300: reading the position before the wait as an
+// address hint for the row, to save that second round trip, was 0.03 to
+// 0.26 us slower per launch from T = 1 to 128, and so was a grid-stride loop
+// over the heads.)
 template <typename T, bool FP8, int LPH, int LAYOUT>
 __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
     constexpr int N = vec_elems<T>();
     constexpr int HPW = 32 / LPH;
     const int lane = threadIdx.x & 31;
     const int sub = lane & (LPH - 1);
-    const int slot = lane / LPH;
-    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    // < 2^31 + 8 HPW: units are at most 2^31 - 1 (validated)
+    const uint32_t u = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * HPW + lane / LPH;
+    const bool active = u < p.units;
+    const Unit un = locate(p, active ? u : 0);
 
     if (threadIdx.x == 0) {
         const uint32_t per_cta = (blockDim.x >> 5) * HPW;
         prefetch_heads(p, blockIdx.x * per_cta, (blockIdx.x + 1) * per_cta, true);
     }
-    // The first pass's position, read before the wait as an address hint for
-    // the cache row.  The preceding grid may still be writing it, so it is
-    // read at L2 (leaving no L1 line behind) and never used as a value: the
-    // row it names is loaded after the wait, next to the position itself,
-    // and kept only if the two positions agree (reloaded otherwise).  The
-    // position and the row then cost one round trip instead of two.
-    int64_t hint = -1;
-    if (p.rot > 0 && warp * HPW + slot < p.units) {
-        hint = __ldcg(reinterpret_cast<const long long*>(p.pos) +
-                      fast_div(warp * HPW + slot, p.heads));
-    }
     pdl_wait();
     pdl_launch_dependents();
 
     const int lane_role = p.rot > 0 ? rotary_role<T, LAYOUT>(p, sub) : 0;
-    for (uint32_t base = warp * HPW; base < p.units; base += nwarps * HPW) {
-        const uint32_t u = base + slot;
-        const bool active = u < p.units;
-        const Unit un = locate(p, active ? u : base);
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        int64_t pos = -1;
-        if (active) {
-            raw = __ldcs(reinterpret_cast<const uint4*>(un.src) + sub);
-            if (p.rot > 0) pos = __ldg(p.pos + un.t);
-        }
-        CacheRegs<T, LAYOUT> cr;
-        const bool hinted = lane_role != 0 && active && hint >= 0 && hint < p.cache_len;
-        if (hinted) load_cache<T, LAYOUT>(p, hint, sub, lane_role, cr);
-        float w[N];
-        weights_plus_delta<T>(p, un.w, sub, w);
-        const bool rot = active && pos >= 0 && pos < p.cache_len;
-        const int role = rot ? lane_role : 0;
-        if (role != 0 && !(hinted && pos == hint)) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
-        hint = -1;  // later passes take no hint
-        qk_core<T, FP8, LPH, LAYOUT>(p, un.dst, active, lane, sub, raw, w, role, cr);
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    int64_t pos = -1;
+    if (active) {
+        raw = __ldcs(reinterpret_cast<const uint4*>(un.src) + sub);
+        if (p.rot > 0) pos = __ldg(p.pos + un.t);
     }
+    float w[N];
+    weights_plus_delta<T>(p, un.w, sub, w);
+    const bool rot = active && pos >= 0 && pos < p.cache_len;
+    const int role = rot ? lane_role : 0;
+    CacheRegs<T, LAYOUT> cr;
+    if (role != 0) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
+    qk_core<T, FP8, LPH, LAYOUT>(p, un.dst, active, lane, sub, raw, w, role, cr);
 }
 
 // ---------------------------------------------------------------- generic path
@@ -176,8 +163,7 @@ cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
             cudaError_t e = launch_qk_quad<T, FP8>(a, p, cfg, &handled);
             if (handled || e != cudaSuccess) return e;
         }
-        const int64_t cap = (int64_t)sms * (2048 / threads) * 64;
-        if (blocks > cap) blocks = cap;
+        // one-shot: units <= 2^31 - 1 (validated), so blocks < 2^28
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(threads);
         cfg.dynamicSmemBytes = 0;

@@ -30,14 +30,20 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
     const QKP& p = a.p;
     const int lane = threadIdx.x & 31;
     const int sub = lane & (LPH - 1);
-    const int slot_in_warp = lane / LPH;
-    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     const int hb = p.D * (int)sizeof(T);
+    // one-shot grid; < 2^31 + 8 HPW since units are at most 2^31 - 1
+    const uint32_t u = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * HPW + lane / LPH;
+    const bool active = u < p.units;
+    const uint32_t t = fast_div(active ? u : 0, a.per_token);
+    const int h = (int)((active ? u : 0) - t * a.per_token.d);
+    const char* src = p.q + (int64_t)t * a.row_bytes + (int64_t)h * hb;
+    const bool isq = h < p.q_heads;
+    const bool isv = h >= p.q_heads + p.k_heads;
+    const int j = isq ? h : (isv ? h - p.q_heads - p.k_heads : h - p.q_heads);
 
     if (threadIdx.x == 0) {
-        // the qkv rows of this CTA's first units into L2 while the preceding
-        // grid drains
+        // the qkv rows of this CTA's units into L2 while the preceding grid
+        // drains
         const uint32_t per_cta = (blockDim.x >> 5) * HPW;
         const uint32_t u0 = blockIdx.x * per_cta;
         const uint32_t u1 = u0 + per_cta < p.units ? u0 + per_cta : p.units;
@@ -46,54 +52,31 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
             prefetch_l2(p.q, t0 * a.row_bytes, t1 * a.row_bytes);
         }
     }
-    // The first pass's position as an address hint for the cache row, read
-    // before the wait at L2 and checked after it (as in the prologue's
-    // lane-group kernel): one round trip for the position and the row.
-    int64_t hint = -1;
-    if (p.rot > 0 && warp * HPW + slot_in_warp < p.units) {
-        hint = __ldcg(reinterpret_cast<const long long*>(p.pos) +
-                      fast_div(warp * HPW + slot_in_warp, a.per_token));
-    }
     pdl_wait();
     pdl_launch_dependents();
 
     const int lane_role = p.rot > 0 ? rotary_role<T, LAYOUT>(p, sub) : 0;
-    for (uint32_t base = warp * HPW; base < p.units; base += nwarps * HPW) {
-        const uint32_t u = base + slot_in_warp;
-        const bool active = u < p.units;
-        const uint32_t t = fast_div(active ? u : base, a.per_token);
-        const int h = (int)((active ? u : base) - t * a.per_token.d);
-        const char* src = p.q + (int64_t)t * a.row_bytes + (int64_t)h * hb;
-        const bool isq = h < p.q_heads;
-        const bool isv = h >= p.q_heads + p.k_heads;
-        const int j = isq ? h : (isv ? h - p.q_heads - p.k_heads : h - p.q_heads);
-
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        int64_t pos = -1, slot = -1;
-        if (active) {
-            raw = __ldcs(reinterpret_cast<const uint4*>(src) + sub);
-            if (p.rot > 0 && !isv) pos = __ldg(p.pos + t);
-            if (!isq && a.slots != nullptr) slot = __ldg(a.slots + t);
-        }
-        CacheRegs<T, LAYOUT> cr;
-        const bool hinted =
-            lane_role != 0 && active && !isv && hint >= 0 && hint < p.cache_len;
-        if (hinted) load_cache<T, LAYOUT>(p, hint, sub, lane_role, cr);
-        char* dst = nullptr;
-        if (isq) {
-            dst = p.qo + ((int64_t)t * p.q_heads + j) * hb;
-        } else if (slot >= 0 && slot < a.num_slots) {
-            dst = (isv ? a.vc : a.kc) + (slot * p.k_heads + j) * hb;
-        }
-        float w[N];
-        weights_plus_delta<T>(p, isq ? p.wq : p.wk, sub, w);
-        const bool rot = active && !isv && pos >= 0 && pos < p.cache_len;
-        const int role = rot ? lane_role : 0;
-        if (role != 0 && !(hinted && pos == hint)) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
-        hint = -1;  // later passes take no hint
-        qk_core<T, false, LPH, LAYOUT>(p, dst, active && dst != nullptr, lane, sub, raw, w, role,
-                                       cr, isv);
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    int64_t pos = -1, slot = -1;
+    if (active) {
+        raw = __ldcs(reinterpret_cast<const uint4*>(src) + sub);
+        if (p.rot > 0 && !isv) pos = __ldg(p.pos + t);
+        if (!isq && a.slots != nullptr) slot = __ldg(a.slots + t);
     }
+    char* dst = nullptr;
+    if (isq) {
+        dst = p.qo + ((int64_t)t * p.q_heads + j) * hb;
+    } else if (slot >= 0 && slot < a.num_slots) {
+        dst = (isv ? a.vc : a.kc) + (slot * p.k_heads + j) * hb;
+    }
+    float w[N];
+    weights_plus_delta<T>(p, isq ? p.wq : p.wk, sub, w);
+    const bool rot = active && !isv && pos >= 0 && pos < p.cache_len;
+    const int role = rot ? lane_role : 0;
+    CacheRegs<T, LAYOUT> cr;
+    if (role != 0) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
+    qk_core<T, false, LPH, LAYOUT>(p, dst, active && dst != nullptr, lane, sub, raw, w, role, cr,
+                                   isv);
 }
 
 // Any head size or alignment: one warp per head, staged in shared memory.
@@ -210,9 +193,7 @@ cudaError_t launch_typed(const QKVArgs& a, QKVP& k, cudaStream_t s, bool* handle
         cudaError_t e = launch_qkv_quad<T>(a, k, cfg, &quad);
         if (quad || e != cudaSuccess) return e;
     }
-    const int64_t cap = (int64_t)sm_count() * (2048 / threads) * 64;
-    if (blocks > cap) blocks = cap;
-    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.gridDim = dim3((unsigned)blocks);  // one-shot: blocks < 2^28
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, vfn, k);

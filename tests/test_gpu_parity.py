@@ -328,12 +328,11 @@ REWRITE_GEOMS = {
 
 @pytest.mark.parametrize("op,geom", [("qk", g) for g in REWRITE_GEOMS] + [("qkv", "bf16_d256_rot64")])
 def test_positions_rewritten_by_the_preceding_kernel(op, geom):
-    # The prologue's lane-group kernels read each token's position before
-    # their dependent-launch wait, as an address hint only, and check it
-    # after the wait.  Here the kernel just before them on the stream (a
-    # residual add whose residual is the positions array) rewrites the
-    # positions while the prologue may already be resident: a stale hint
-    # must cost a reload, never a wrong row.
+    # The kernel just before the prologue on the stream (a residual add whose
+    # residual is the positions array) rewrites the positions while the
+    # prologue's CTAs may already be resident, computing addresses and
+    # prefetching before their dependent-launch wait: every position and
+    # cache row must still be read after the wait.
     dtype, Hq, Hk, D, rot, layout = REWRITE_GEOMS[geom]
     T, P = 12, 200
     old = np.array([5, 6, 7, 250, 9, 10, 11, 12, 13, 14, 15, 16], np.int64)

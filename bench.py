@@ -716,18 +716,35 @@ def sweep(torch, ops, synth, device, peak):
     return out
 
 
+ALIAS = {
+    "qk_norm_rope_bf16_16x2_d256_r64": "qk16x2", "qk_norm_rope_bf16_24x4_d256_r64": "qk24x4",
+    "qk_norm_rope_dflash2_bf16_32x32_d128_inplace_W16": "dflash2",
+    "add_rmsnorm_bf16_h2048": "arn2048", "add_rmsnorm_bf16_h2048_fp8": "arn2048f8",
+    "add_rmsnorm_bf16_h1024": "arn1024", "add_rmsnorm_bf16_h1024_fp8": "arn1024f8",
+    "add_rmsnorm_bf16_h2560": "arn2560", "add_rmsnorm_bf16_h2560_fp8": "arn2560f8",
+    "rmsnorm_noweight_bf16_h2048_fp8": "rmsnw2048f8", "rope_bf16_24x4_d256_r64": "rope24x4",
+    "layernorm_bf16_h1152": "ln1152", "quantize_fp8_bf16_rows_x2048": "quant2048",
+    "qkv_rope_cache_bf16_16x2_d256_r64": "qkv16x2", "glu_silu_bf16_d9728": "silu9728",
+    "glu_gelu_bf16_d2048_fp8": "gelu2048f8", "glu_gelu_bf16_d10240": "gelu10240"}
+T1_ALIAS = {"qk_norm_rope_16x2": "qk16x2", "qk_norm_rope_24x4": "qk24x4",
+            "add_rmsnorm_h2560": "arn2560", "glu_silu_d9728": "silu9728",
+            "launch_floor_quantize_16": "floor"}
+
+
 def sweep_summary(sw, t1):
-    """The key figures of the sweep in a few hundred bytes: per op, the
-    fraction of measured HBM peak and of the same-bytes copy at T = 256, 512
-    and the largest T; and the T = 1 microseconds per call."""
+    """The key figures of the sweep in under 1.5 KB (the end of the JSON line):
+    per op, the fraction of measured HBM peak and of the same-bytes copy at
+    T = 256, 512 and the largest T, as "T:peak/copy"; and the T = 1
+    microseconds per call."""
     rows = {}
     for key, by_t in sw.items():
         ts = list(by_t)
         pick = [t for t in ts if t in ("256", "512", "B16", "B64")] + [ts[-1]]
-        rows[key] = {t: [by_t[t][2], by_t[t][5]] for t in dict.fromkeys(pick)}
-    return {"format": "op -> T -> [fraction of measured HBM peak, fraction of the same-bytes "
-                      "copy's speed]; t1: median us per call, graph replay, warm L2",
-            "t1": {k: v["median"] for k, v in (t1 or {}).items() if "median" in v},
+        rows[ALIAS.get(key, key)] = " ".join(
+            f"{t}:{by_t[t][2]:.2f}/{by_t[t][5]:.2f}" for t in dict.fromkeys(pick))
+    return {"format": "T:fraction of HBM peak/fraction of copy speed",
+            "t1_us": {T1_ALIAS.get(k, k): v["median"] for k, v in (t1 or {}).items()
+                      if "median" in v},
             "ops": rows}
 
 

@@ -567,18 +567,14 @@ def capture(torch, fn, stream):
 
 
 def source_sha(kernel):
-    """Hash of the kernel's own source text (its template through the closing
-    brace at column 0) and of the shared device helpers it calls, so that
-    edits elsewhere in its file leave a stored capture valid."""
+    """Hash of the source file that holds the kernel and of the shared device
+    helpers it includes, so that a stored capture goes stale whenever the
+    kernel's code may have changed."""
     csrc = os.path.join(ROOT, "memory_bound_decode_qk_gb300", "csrc")
-    with open(os.path.join(csrc, OP_SOURCE[kernel])) as f:
-        text = f.read()
-    at = text.index(f" {kernel}(")
-    start = text.rindex("\ntemplate <", 0, at) + 1
-    end = text.index("\n}\n", at) + 3
-    h = hashlib.sha256(text[start:end].encode())
-    with open(os.path.join(csrc, "edge_common.cuh"), "rb") as f:
-        h.update(f.read())
+    h = hashlib.sha256()
+    for name in (OP_SOURCE[kernel], "edge_common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 

@@ -68,17 +68,19 @@ def gate_error_coefficients(act):
     t = e^-|v| comes from ex2.approx of -|v| log2(e).  A relative error e of
     that argument is an absolute error |v| e of the exponent, so t carries a
     relative error |v| e plus the instruction's 4u.  SiLU: e = 1.5u (the
-    constant log2(e) and the product).  tanh-GELU: v = K g (1 + C g^2) carries
-    6u (the constants K and C, the products C g, (C g) g, K g and the final
-    product, the sum 1 + C g^2), then 1.5u more for -|v| log2(e): e = 7.5u.
+    constant log2(e) and the product).  tanh-GELU: the exponent is formed as
+    v log2(e) = K' g (1 + C g^2) with K' = 2 sqrt(2/pi) log2(e) rounded once:
+    the constants K' and C (u/2 each), the products C g, (C g) g, K' g and
+    the final product (u each), and the rounding of the sum 1 + C g^2 (u; it
+    cannot cancel, since C g^2 >= 0): e = 6u.
     sigma = num / (1 + t) takes the add and rcp.approx (3u); the output
     g * u * sigma three products (3u).  Constant part: 4 + 3 + 3 = 10.
     """
-    return (10.0, 1.5) if act == 0 else (10.0, 7.5)
+    return (10.0, 1.5) if act == 0 else (10.0, 6.0)
 
 
 # The gate bands: the coefficients above, the |v| term rounded up (SiLU 1.5 to
-# 2, tanh-GELU 7.5 to 8).
+# 2, tanh-GELU 6 to 8).
 GATE_BAND = {0: (10.0, 2.0), 1: (10.0, 8.0)}
 
 

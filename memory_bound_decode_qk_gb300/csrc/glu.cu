@@ -81,6 +81,26 @@ __device__ __forceinline__ float gate_fast(float g, float u) {
     return __fmul_rn(__fmul_rn(g, __fmul_rn(num, rcp_approx_1to2(__fadd_rn(1.0f, t)))), u);
 }
 
+// gate_fast on a pair of elements: the products and sums as packed two-lane
+// instructions (each lane rounded as gate_fast rounds it, so the results are
+// the same bits), the exponential and the reciprocal per lane.
+template <int ACT>
+__device__ __forceinline__ float2 gate_fast2(float2 g, float2 u) {
+    float2 vl;
+    if constexpr (ACT == kSilu) {
+        vl = __fmul2_rn(g, splat2(kLog2e));
+    } else {
+        const float2 c2 = __fmul2_rn(__fmul2_rn(splat2(kC), g), g);
+        vl = __fmul2_rn(__fmul2_rn(splat2(kK2L), g), __fadd2_rn(splat2(1.0f), c2));
+    }
+    const float2 t = make_float2(ex2_approx(-fabsf(vl.x)), ex2_approx(-fabsf(vl.y)));
+    const float2 num = make_float2(vl.x >= 0.0f ? 1.0f : t.x, vl.y >= 0.0f ? 1.0f : t.y);
+    const float2 den = __fadd2_rn(splat2(1.0f), t);
+    const float2 rc = make_float2(rcp_approx_1to2(den.x), rcp_approx_1to2(den.y));
+    // g * sigma(v) first, u last (see gate_fast)
+    return __fmul2_rn(__fmul2_rn(g, __fmul2_rn(num, rc)), u);
+}
+
 // act(g) * u, accurate form (fp32 outputs).
 template <int ACT>
 __device__ __forceinline__ float gate_accurate(float g, float u) {
@@ -188,16 +208,26 @@ __global__ void __launch_bounds__(256) glu_vec_kernel(GluP p) {
         for (int k = 0; k < U; ++k) {
             const uint32_t i = b0 + k * blockDim.x;
             if (i >= p.total) continue;
-            float g[N], u[N], y[N];
-            unpack_vec<T, N>(gv[k], g);
-            unpack_vec<T, N>(uv[k], u);
+            if constexpr (std::is_same<T, float>::value && !FP8) {
+                float g[N], u[N], y[N];
+                unpack_vec<T, N>(gv[k], g);
+                unpack_vec<T, N>(uv[k], u);
 #pragma unroll
-            for (int e = 0; e < N; ++e) y[e] = gate<T, FP8, ACT>(g[e], u[e]);
-            if constexpr (FP8) {
-                auto q8 = quantize_vec<N>(y, p.inv);
-                reinterpret_cast<decltype(q8)*>(p.out)[i] = q8;
-            } else {
+                for (int e = 0; e < N; ++e) y[e] = gate_accurate<ACT>(g[e], u[e]);
                 reinterpret_cast<uint4*>(p.out)[i] = pack_vec<T, N>(y);
+            } else {
+                // the fast form on element pairs
+                float2 g[N / 2], u[N / 2], y[N / 2];
+                unpack_pairs<T, N>(gv[k], g);
+                unpack_pairs<T, N>(uv[k], u);
+#pragma unroll
+                for (int j = 0; j < N / 2; ++j) y[j] = gate_fast2<ACT>(g[j], u[j]);
+                if constexpr (FP8) {
+                    auto q8 = quantize_pairs<N>(y, p.inv);
+                    reinterpret_cast<decltype(q8)*>(p.out)[i] = q8;
+                } else {
+                    reinterpret_cast<uint4*>(p.out)[i] = pack_pairs<T, N>(y);
+                }
             }
         }
     }

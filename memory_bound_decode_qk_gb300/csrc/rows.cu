@@ -99,54 +99,58 @@ __global__ void __launch_bounds__(512) rows_vec_kernel(RowsP p) {
         wr[i] = (ok && wv != nullptr) ? __ldg(wv + idx) : make_uint4(0u, 0u, 0u, 0u);
     }
 
-    // beyond 32 terms per thread, two running sums alternating by vector
-    // (at most 4N sequential terms each, for the error bound of the
-    // tolerance)
+    // running sums: the two lanes of a pair, and beyond 32 terms per thread
+    // two pairs alternating by vector (at most 2N sequential terms each, for
+    // the error bound of the tolerance)
+    constexpr int P = N / 2;
     constexpr bool kSplit = V * N > 32;
-    float ssp[2] = {0.0f, 0.0f};
+    float2 ssp[2] = {splat2(0.0f), splat2(0.0f)};
 #pragma unroll
     for (int i = 0; i < V; ++i) {
-        float a[N];
-        unpack_vec<T, N>(xv[i], a);
+        float2 a[P];
+        unpack_pairs<T, N>(xv[i], a);
         if constexpr (ADD) {
             // eager semantics: widen, add in fp32, round once to the dtype
-            float b[N];
-            unpack_vec<T, N>(rv[i], b);
+            float2 b[P];
+            unpack_pairs<T, N>(rv[i], b);
 #pragma unroll
-            for (int e = 0; e < N; ++e) a[e] = round_to<T>(__fadd_rn(a[e], b[e]));
-            xv[i] = pack_vec<T, N>(a);
+            for (int j = 0; j < P; ++j) a[j] = __fadd2_rn(a[j], b[j]);
+            xv[i] = pack_pairs<T, N>(a);
+            unpack_pairs<T, N>(xv[i], a);  // the rounded sums
             const int idx = tid + i * tpr;
             if (active && idx < p.nvec) rr[idx] = xv[i];
         }
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-            ssp[kSplit ? (i & 1) : 0] = __fmaf_rn(a[e], a[e], ssp[kSplit ? (i & 1) : 0]);
+        for (int j = 0; j < P; ++j) {
+            ssp[kSplit ? (i & 1) : 0] = __ffma2_rn(a[j], a[j], ssp[kSplit ? (i & 1) : 0]);
         }
     }
-    const float ss = row_sum(kSplit ? __fadd_rn(ssp[0], ssp[1]) : ssp[0], red);
-    const float r = inv_rms(ss, p.invH, p.eps);
+    const float2 s2 = kSplit ? __fadd2_rn(ssp[0], ssp[1]) : ssp[0];
+    const float ss = row_sum(__fadd_rn(s2.x, s2.y), red);
+    const float2 r2 = splat2(inv_rms(ss, p.invH, p.eps));
+    const float2 delta2 = splat2(p.delta);
 
     char* orow = p.out + rsafe * out_row;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
         const int idx = tid + i * tpr;
         if (!(active && idx < p.nvec)) continue;
-        float s[N], y[N];
-        unpack_vec<T, N>(xv[i], s);
+        float2 sv[P], y[P];
+        unpack_pairs<T, N>(xv[i], sv);
         if (wv != nullptr) {
-            float w[N];
-            unpack_vec<T, N>(wr[i], w);
+            float2 w[P];
+            unpack_pairs<T, N>(wr[i], w);
 #pragma unroll
-            for (int e = 0; e < N; ++e) y[e] = __fmul_rn(__fmul_rn(s[e], r), __fadd_rn(w[e], p.delta));
+            for (int j = 0; j < P; ++j) y[j] = __fmul2_rn(__fmul2_rn(sv[j], r2), __fadd2_rn(w[j], delta2));
         } else {
 #pragma unroll
-            for (int e = 0; e < N; ++e) y[e] = __fmul_rn(s[e], r);
+            for (int j = 0; j < P; ++j) y[j] = __fmul2_rn(sv[j], r2);
         }
         if constexpr (FP8) {
-            auto q8 = quantize_vec<N>(y, p.inv);
+            auto q8 = quantize_pairs<N>(y, p.inv);
             reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
         } else {
-            reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
+            reinterpret_cast<uint4*>(orow)[idx] = pack_pairs<T, N>(y);
         }
     }
 }
@@ -301,19 +305,22 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
 // CTA in shared memory, so the output loop reads them without global latency
 // and they hold no registers across the reductions.  A lane holds
 // V = ceil(vectors / 32) <= 8 vectors, so few registers are live and many
-// rows are in flight per SM.
-// Register budget: 4 CTAs per SM (64 registers) up to 4 vectors per lane, 3
-// (85) at 5 and 2 (128) beyond, the counts at which ptxas for sm_103a keeps
-// the variants spill-free (the 16-bit FP8 ones at 4 vectors spill under 32
-// bytes).
+// rows are in flight per SM.  The elementwise steps run on fp32 pairs.
+// Register budget, in CTAs of the 128 threads launched per SM: 8 (64
+// registers) up to 4 vectors per lane, 7 (72) at 5 and 4 (128) beyond, the
+// counts at which ptxas for sm_103a keeps the variants spill-free.  At 5
+// vectors (width 1152) 7 CTAs per SM hold the 1024 CTAs of T = 4096 in one
+// wave (1064 slots); a variant held to 6 (78 registers) measured 1.27x
+// slower there.
 template <int V>
 constexpr int ln_warp_min_blocks() {
-    return V <= 4 ? 4 : V == 5 ? 3 : 2;
+    return V <= 4 ? 8 : V == 5 ? 7 : 4;
 }
 
 template <typename T, bool FP8, int V>
-__global__ void __launch_bounds__(256, ln_warp_min_blocks<V>()) ln_warp_kernel(RowsP p) {
+__global__ void __launch_bounds__(128, ln_warp_min_blocks<V>()) ln_warp_kernel(RowsP p) {
     constexpr int N = vec_elems<T>();
+    constexpr int P = N / 2;
     extern __shared__ __align__(16) uint4 ln_gb[];  // gamma [nvec], then beta [nvec]
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
@@ -359,55 +366,59 @@ __global__ void __launch_bounds__(256, ln_warp_min_blocks<V>()) ln_warp_kernel(R
             __syncthreads();
             staged = true;
         }
-        // beyond 32 terms per thread, two running sums alternating by vector
+        // running sums: the two lanes of a pair, and beyond 32 terms per
+        // thread two pairs alternating by vector
         constexpr bool kSplit = V * N > 32;
-        float sp[2] = {0.0f, 0.0f};
+        float2 sp[2] = {splat2(0.0f), splat2(0.0f)};
 #pragma unroll
         for (int i = 0; i < V; ++i) {
-            float a[N];
-            unpack_vec<T, N>(xv[i], a);
+            float2 a[P];
+            unpack_pairs<T, N>(xv[i], a);
 #pragma unroll
-            for (int e = 0; e < N; ++e) {
-                sp[kSplit ? (i & 1) : 0] = __fadd_rn(sp[kSplit ? (i & 1) : 0], a[e]);
+            for (int j = 0; j < P; ++j) {
+                sp[kSplit ? (i & 1) : 0] = __fadd2_rn(sp[kSplit ? (i & 1) : 0], a[j]);
             }
         }
-        const float sum = kSplit ? __fadd_rn(sp[0], sp[1]) : sp[0];
-        const float mu = __fmul_rn(group_sum<32>(sum), p.invH);
-        float sqp[2] = {0.0f, 0.0f};
+        const float2 s2 = kSplit ? __fadd2_rn(sp[0], sp[1]) : sp[0];
+        const float mu = __fmul_rn(group_sum<32>(__fadd_rn(s2.x, s2.y)), p.invH);
+        const float2 nmu = splat2(-mu);  // x + (-mu) is x - mu exactly
+        float2 sqp[2] = {splat2(0.0f), splat2(0.0f)};
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             if (lane + 32 * i >= p.nvec) continue;  // padding lanes add nothing
-            float a[N];
-            unpack_vec<T, N>(xv[i], a);
+            float2 a[P];
+            unpack_pairs<T, N>(xv[i], a);
 #pragma unroll
-            for (int e = 0; e < N; ++e) {
-                const float d = __fsub_rn(a[e], mu);
-                sqp[kSplit ? (i & 1) : 0] = __fmaf_rn(d, d, sqp[kSplit ? (i & 1) : 0]);
+            for (int j = 0; j < P; ++j) {
+                const float2 d = __fadd2_rn(a[j], nmu);
+                sqp[kSplit ? (i & 1) : 0] = __ffma2_rn(d, d, sqp[kSplit ? (i & 1) : 0]);
             }
         }
-        const float sq = kSplit ? __fadd_rn(sqp[0], sqp[1]) : sqp[0];
-        const float r = inv_rms(group_sum<32>(sq), p.invH, p.eps);
+        const float2 q2 = kSplit ? __fadd2_rn(sqp[0], sqp[1]) : sqp[0];
+        const float r = inv_rms(group_sum<32>(__fadd_rn(q2.x, q2.y)), p.invH, p.eps);
         if (!active) continue;
+        const float2 r2 = splat2(r);
         char* orow = p.out + row * out_row;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int idx = lane + 32 * i;
             if (idx >= p.nvec) continue;
-            float a[N], gg[N], bb[N], y[N];
-            unpack_vec<T, N>(xv[i], a);
-            if (gv != nullptr) unpack_vec<T, N>(gs[idx], gg);
-            if (bv != nullptr) unpack_vec<T, N>(bs[idx], bb);
+            float2 a[P], gg[P], bb[P], y[P];
+            unpack_pairs<T, N>(xv[i], a);
+            if (gv != nullptr) unpack_pairs<T, N>(gs[idx], gg);
+            if (bv != nullptr) unpack_pairs<T, N>(bs[idx], bb);
 #pragma unroll
-            for (int e = 0; e < N; ++e) {
-                const float d = __fsub_rn(a[e], mu);
-                const float rg = gv != nullptr ? __fmul_rn(r, gg[e]) : r;
-                y[e] = bv != nullptr ? __fmaf_rn(d, rg, bb[e]) : __fmul_rn(d, rg);
+            for (int j = 0; j < P; ++j) {
+                // (x - mu) (r gamma) + beta: one product and one fma per pair
+                const float2 d = __fadd2_rn(a[j], nmu);
+                const float2 rg = gv != nullptr ? __fmul2_rn(r2, gg[j]) : r2;
+                y[j] = bv != nullptr ? __ffma2_rn(d, rg, bb[j]) : __fmul2_rn(d, rg);
             }
             if constexpr (FP8) {
-                auto q8 = quantize_vec<N>(y, p.inv);
+                auto q8 = quantize_pairs<N>(y, p.inv);
                 reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
             } else {
-                reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
+                reinterpret_cast<uint4*>(orow)[idx] = pack_pairs<T, N>(y);
             }
         }
     }

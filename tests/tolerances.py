@@ -28,27 +28,26 @@ import numpy as np
 U = 2.0 ** -24
 
 # Largest reduction shapes of the kernels' fp32 sums of squares (a thread's
-# sequential terms, the merge of its two alternating sums, the shuffle tree of
-# a warp, the combine over the warps of a row, the combine over the CTAs of a
-# cluster).  Every term is non-negative, so each addition adds at most u of
-# the total to the relative error of the sum.
+# sequential terms; the merges of its two alternating sums and of the two
+# lanes of an fp32 pair; the shuffle tree of a warp; the combine over the
+# warps of a row).  Every term is non-negative, so each addition adds at most
+# u of the total to the relative error of the sum.
 MAX_SEQ_TERMS = 32      # at most 4 vectors of 8 elements per running sum
-MAX_TREE_LEVELS = 1 + 5  # the two-sum merge, then a 32-lane xor tree
+MAX_TREE_LEVELS = 2 + 5  # the two merges, then a 32-lane xor tree
 MAX_WARPS_PER_ROW = 16
-MAX_CLUSTER_CTAS = 8
 
 
 def rms_norm_error_u(seq_terms=MAX_SEQ_TERMS, tree_levels=MAX_TREE_LEVELS,
-                     warps=MAX_WARPS_PER_ROW, ctas=MAX_CLUSTER_CTAS):
+                     warps=MAX_WARPS_PER_ROW):
     """Worst-case relative error, in u, of the fp32 normalized value
     x * r * (w + delta) with r = rsqrtf(fma(ss, 1/n, eps)).
 
-      ss:          (seq_terms + tree_levels + warps - 1 + ctas - 1) u;
+      ss:          (seq_terms + tree_levels + warps - 1) u;
       r:           half of the error of its argument (ss, the rounding of 1/n
                    and of the fma: ss + 2u), plus rsqrtf's 4u;
       the output:  w + delta, x * r and the product with the weight: 3u.
     """
-    ss = seq_terms + tree_levels + (warps - 1) + (ctas - 1)
+    ss = seq_terms + tree_levels + (warps - 1)
     return 0.5 * (ss + 2) + 4 + 3
 
 

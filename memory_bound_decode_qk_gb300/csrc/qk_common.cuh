@@ -161,43 +161,49 @@ __device__ __forceinline__ void qk_core(const QKP& p, char* dst, bool active, in
                                         const uint4& raw, const float (&w)[vec_elems<T>()], int role,
                                         const CacheRegs<T, LAYOUT>& cr, bool copy = false) {
     constexpr int N = vec_elems<T>();
-    float x[N];
-    unpack_vec<T, N>(raw, x);
+    constexpr int P = N / 2;
+    // the elementwise steps on fp32 pairs (packed two-lane instructions, each
+    // lane rounded as the scalar form rounds it)
+    float2 x[P];
+    unpack_pairs<T, N>(raw, x);
     // normalized value n (fp32); without normalization n = x
-    float n[N];
+    float2 n[P];
     if (p.mode & kModeNorm) {
-        float ss = 0.0f;
+        float2 s2 = splat2(0.0f);
 #pragma unroll
-        for (int i = 0; i < N; ++i) ss = __fmaf_rn(x[i], x[i], ss);
-        ss = group_sum<LPH>(ss);
-        const float r = inv_rms(ss, p.invD, p.eps);
+        for (int j = 0; j < P; ++j) s2 = __ffma2_rn(x[j], x[j], s2);
+        const float ss = group_sum<LPH>(__fadd_rn(s2.x, s2.y));
+        const float2 r2 = splat2(inv_rms(ss, p.invD, p.eps));
 #pragma unroll
-        for (int i = 0; i < N; ++i) n[i] = copy ? x[i] : __fmul_rn(__fmul_rn(x[i], r), w[i]);
+        for (int j = 0; j < P; ++j) {
+            n[j] = copy ? x[j] : __fmul2_rn(__fmul2_rn(x[j], r2), make_float2(w[2 * j], w[2 * j + 1]));
+        }
     } else {
 #pragma unroll
-        for (int i = 0; i < N; ++i) n[i] = x[i];
+        for (int j = 0; j < P; ++j) n[j] = x[j];
     }
-    // m: n rounded to the activation dtype.  The rotation consumes m, or n
-    // itself in the unrounded mode; channels that do not rotate emit m.
+    // m: n rounded to the activation dtype (packed exactly as `mine`).  The
+    // rotation consumes m, or n itself in the unrounded mode; channels that
+    // do not rotate emit m.
     const bool unrounded = (p.mode & kModeUnrounded) != 0;
-    float m[N], src[N];
+    const uint4 mine = pack_pairs<T, N>(n);
+    float2 m[P], src[P];
+    unpack_pairs<T, N>(mine, m);
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        m[i] = round_to<T>(n[i]);
-        src[i] = unrounded ? n[i] : m[i];
-    }
+    for (int j = 0; j < P; ++j) src[j] = unrounded ? n[j] : m[j];
 
-    float y[N];
+    float2 y[P];
 #pragma unroll
-    for (int i = 0; i < N; ++i) y[i] = m[i];
+    for (int j = 0; j < P; ++j) y[j] = m[j];
 
     if constexpr (LAYOUT == kInterleaved) {
         if (role != 0) {
+            // pair (a, b) -> (a c - b s, b c + a s): the products
+            // (b, a) * (-s, s), then one fma per pair
 #pragma unroll
-            for (int i = 0; i < N / 2; ++i) {
-                const float a = src[2 * i], b = src[2 * i + 1];
-                y[2 * i] = __fmaf_rn(a, cr.c[i], -__fmul_rn(b, cr.s[i]));
-                y[2 * i + 1] = __fmaf_rn(b, cr.c[i], __fmul_rn(a, cr.s[i]));
+            for (int j = 0; j < P; ++j) {
+                const float2 t = __fmul2_rn(make_float2(src[j].y, src[j].x), make_float2(-cr.s[j], cr.s[j]));
+                y[j] = __ffma2_rn(src[j], splat2(cr.c[j]), t);
             }
         }
     } else {
@@ -205,34 +211,39 @@ __device__ __forceinline__ void qk_core(const QKP& p, char* dst, bool active, in
         // held by the lane half/N positions away in the same lane group
         const int hv = p.half / N;
         const int from = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
-        float pm[N];
+        float2 pm[P];
         if (unrounded) {
 #pragma unroll
-            for (int i = 0; i < N; ++i) pm[i] = __shfl_sync(0xffffffffu, src[i], from);
+            for (int j = 0; j < P; ++j) {
+                pm[j].x = __shfl_sync(0xffffffffu, src[j].x, from);
+                pm[j].y = __shfl_sync(0xffffffffu, src[j].y, from);
+            }
         } else {
-            const uint4 mine = pack_vec<T, N>(m);  // exact: m is already rounded to T
             uint4 other;
             other.x = __shfl_sync(0xffffffffu, mine.x, from);
             other.y = __shfl_sync(0xffffffffu, mine.y, from);
             other.z = __shfl_sync(0xffffffffu, mine.z, from);
             other.w = __shfl_sync(0xffffffffu, mine.w, from);
-            unpack_vec<T, N>(other, pm);
+            unpack_pairs<T, N>(other, pm);
         }
-        if (role == 1) {
+        if (role != 0) {
+            // first member: x c - x' s; second: x c + x' s (the sine's sign
+            // folded into the product, which rounds symmetrically)
+            const float sg = role == 1 ? -1.0f : 1.0f;
 #pragma unroll
-            for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(src[i], cr.c[i], -__fmul_rn(pm[i], cr.s[i]));
-        } else if (role == 2) {
-#pragma unroll
-            for (int i = 0; i < N; ++i) y[i] = __fmaf_rn(src[i], cr.c[i], __fmul_rn(pm[i], cr.s[i]));
+            for (int j = 0; j < P; ++j) {
+                const float2 sn = make_float2(sg * cr.s[2 * j], sg * cr.s[2 * j + 1]);
+                y[j] = __ffma2_rn(src[j], make_float2(cr.c[2 * j], cr.c[2 * j + 1]), __fmul2_rn(pm[j], sn));
+            }
         }
     }
 
     if (active) {
         if constexpr (FP8) {
-            auto q8 = quantize_vec<N>(y, p.inv);
+            auto q8 = quantize_pairs<N>(y, p.inv);
             reinterpret_cast<decltype(q8)*>(dst)[sub] = q8;
         } else {
-            reinterpret_cast<uint4*>(dst)[sub] = pack_vec<T, N>(y);
+            reinterpret_cast<uint4*>(dst)[sub] = pack_pairs<T, N>(y);
         }
     }
 }

@@ -21,7 +21,7 @@
 // Units are ordered token-major, so the warps of a CTA share cos/sin rows and
 // the norm weights.  Streamed inputs use evict-first loads.
 // Many heads: the four-threads-per-head path (qk_quad.cu) takes over past a
-// measured fraction of one wave of this path's grid (quad_min_waves).
+// measured number of waves of this path's grid (quad_min_waves).
 // Generic path: one warp per head, staged through shared memory.  It serves
 // any head_dim up to 2048, any even rotary_dim and any element-aligned
 // pointer.
@@ -153,8 +153,9 @@ cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
         const int64_t per_block = (int64_t)(threads / 32) * hpw;
         int64_t blocks = ((int64_t)p.units + per_block - 1) / per_block;
         // Measured on GB300 for every geometry: the one-shot grid wins up to a
-        // geometry's fraction of one wave of resident CTAs; past that, four
-        // threads per head (about 4x fewer instructions per head) win.
+        // measured number of waves of resident CTAs (one for 16-bit heads,
+        // two for fp32); past that, four threads per head (about 4x fewer
+        // instructions per head) win.
         const int64_t hbytes = (int64_t)D * (int64_t)sizeof(T);
         const double wave = (double)resident_ctas((const void*)vfn, threads) * sms *
                             quad_min_waves((int)sizeof(T), a.layout, a.rotary_dim, hbytes);

@@ -568,16 +568,20 @@ cudaError_t launch_qkv_quad(const QKVArgs& a, const QKVP& k, cudaLaunchConfig_t 
 }
 
 double quad_min_waves(int elem_bytes, int layout, int rotary_dim, int64_t head_bytes) {
-    // Measured on GB300 (lane-group against four threads per head, T = 1 to
-    // 4096, with 16- or 32-head CTAs): 16-bit 256- and 512-byte heads with at
-    // most two rotate-half chunks per thread cross at about half a wave of
-    // the lane-group grid (text profiles, FP8 out, DFlash2, context-K);
-    // 16-bit 512-byte heads rotating fully at one wave; fp32 heads at about
-    // one and a half.  Unmeasured geometries keep one wave.
-    if (elem_bytes == 4) return 1.5;
-    const bool heavy = head_bytes == 512 && (layout == kInterleaved || rotary_dim > 64);
-    if ((head_bytes == 256 || head_bytes == 512) && !heavy) return 0.5;
-    return 1.0;
+    // Measured on GB300, lane-group against four threads per head, T = 64 to
+    // 2048 in back-to-back cold launches, for the text profiles (with and
+    // without FP8 output), DFlash2, context-K, 16-bit 512-byte heads rotating
+    // fully and fp32 heads of 128: every 16-bit geometry crosses at about one
+    // wave of the lane-group grid, fp32 heads at about two.  With each buffer
+    // set's own cos/sin cache the lane group wins by 3-10% up to 0.9 of a
+    // wave; with one cache shared by every set (its rows L2-resident, as when
+    // the layers of a step share the positions) the four-thread path wins
+    // the (16,2) text profile by 4-5% from 0.57 of a wave, the one point where
+    // the two disagree.
+    (void)layout;
+    (void)rotary_dim;
+    (void)head_bytes;
+    return elem_bytes == 4 ? 2.0 : 1.0;
 }
 
 bool quad_suits(int layout, int rotary_dim, int64_t head_bytes) {

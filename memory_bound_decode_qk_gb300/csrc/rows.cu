@@ -236,35 +236,38 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
         const bool ok = active && idx < p.nvec;
         xv[i] = ok ? __ldcs(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
     }
-    // beyond 32 terms per thread, two running sums alternating by vector
+    // running sums: the two lanes of a pair, and beyond 32 terms per thread
+    // two pairs alternating by vector
+    constexpr int P = N / 2;
     constexpr bool kSplit = V * N > 32;
-    float sp[2] = {0.0f, 0.0f};
+    float2 sp[2] = {splat2(0.0f), splat2(0.0f)};
 #pragma unroll
     for (int i = 0; i < V; ++i) {
-        float a[N];
-        unpack_vec<T, N>(xv[i], a);
+        float2 a[P];
+        unpack_pairs<T, N>(xv[i], a);
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-            sp[kSplit ? (i & 1) : 0] = __fadd_rn(sp[kSplit ? (i & 1) : 0], a[e]);
+        for (int j = 0; j < P; ++j) {
+            sp[kSplit ? (i & 1) : 0] = __fadd2_rn(sp[kSplit ? (i & 1) : 0], a[j]);
         }
     }
-    const float sum = kSplit ? __fadd_rn(sp[0], sp[1]) : sp[0];
-    const float mu = __fmul_rn(row_sum(sum, red_mu), p.invH);
-    float sqp[2] = {0.0f, 0.0f};
+    const float2 s2 = kSplit ? __fadd2_rn(sp[0], sp[1]) : sp[0];
+    const float mu = __fmul_rn(row_sum(__fadd_rn(s2.x, s2.y), red_mu), p.invH);
+    const float2 nmu = splat2(-mu);  // x + (-mu) is x - mu exactly
+    float2 sqp[2] = {splat2(0.0f), splat2(0.0f)};
 #pragma unroll
     for (int i = 0; i < V; ++i) {
         const int idx = tid + i * tpr;
         if (!(active && idx < p.nvec)) continue;  // padding lanes add nothing
-        float a[N];
-        unpack_vec<T, N>(xv[i], a);
+        float2 a[P];
+        unpack_pairs<T, N>(xv[i], a);
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-            const float d = __fsub_rn(a[e], mu);
-            sqp[kSplit ? (i & 1) : 0] = __fmaf_rn(d, d, sqp[kSplit ? (i & 1) : 0]);
+        for (int j = 0; j < P; ++j) {
+            const float2 d = __fadd2_rn(a[j], nmu);
+            sqp[kSplit ? (i & 1) : 0] = __ffma2_rn(d, d, sqp[kSplit ? (i & 1) : 0]);
         }
     }
-    const float sq = kSplit ? __fadd_rn(sqp[0], sqp[1]) : sqp[0];
-    const float r = inv_rms(row_sum(sq, red_var), p.invH, p.eps);
+    const float2 q2 = kSplit ? __fadd2_rn(sqp[0], sqp[1]) : sqp[0];
+    const float2 r2 = splat2(inv_rms(row_sum(__fadd_rn(q2.x, q2.y), red_var), p.invH, p.eps));
     // gamma and beta (L1/L2-resident), all issued before the output loop
     uint4 gr[V], br[V];
 #pragma unroll
@@ -279,22 +282,22 @@ __global__ void __launch_bounds__(512) ln_vec_kernel(RowsP p) {
     for (int i = 0; i < V; ++i) {
         const int idx = tid + i * tpr;
         if (!(active && idx < p.nvec)) continue;
-        float a[N], gg[N], bb[N], y[N];
-        unpack_vec<T, N>(xv[i], a);
-        if (gv != nullptr) unpack_vec<T, N>(gr[i], gg);
-        if (bv != nullptr) unpack_vec<T, N>(br[i], bb);
+        float2 a[P], gg[P], bb[P], y[P];
+        unpack_pairs<T, N>(xv[i], a);
+        if (gv != nullptr) unpack_pairs<T, N>(gr[i], gg);
+        if (bv != nullptr) unpack_pairs<T, N>(br[i], bb);
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-            // (x - mu) (r gamma) + beta: one product and one fma per element
-            const float d = __fsub_rn(a[e], mu);
-            const float rg = gv != nullptr ? __fmul_rn(r, gg[e]) : r;
-            y[e] = bv != nullptr ? __fmaf_rn(d, rg, bb[e]) : __fmul_rn(d, rg);
+        for (int j = 0; j < P; ++j) {
+            // (x - mu) (r gamma) + beta: one product and one fma per pair
+            const float2 d = __fadd2_rn(a[j], nmu);
+            const float2 rg = gv != nullptr ? __fmul2_rn(r2, gg[j]) : r2;
+            y[j] = bv != nullptr ? __ffma2_rn(d, rg, bb[j]) : __fmul2_rn(d, rg);
         }
         if constexpr (FP8) {
-            auto q8 = quantize_vec<N>(y, p.inv);
+            auto q8 = quantize_pairs<N>(y, p.inv);
             reinterpret_cast<decltype(q8)*>(orow)[idx] = q8;
         } else {
-            reinterpret_cast<uint4*>(orow)[idx] = pack_vec<T, N>(y);
+            reinterpret_cast<uint4*>(orow)[idx] = pack_pairs<T, N>(y);
         }
     }
 }
@@ -529,10 +532,11 @@ cudaError_t launch_typed(const RowsArgs& a, RowsP& p, cudaStream_t s) {
     const bool vec = vec_shape<T, FP8>(a, sms, v);
     if (vec) p.nvec = v.nvec;
     // LayerNorm: one warp per row once there are many rows.  Measured
-    // crossover on GB300: T = 768 at width 1152 (5 vectors per lane), T = 1536
-    // at width 2048 (8 vectors per lane, fewer CTAs per SM)
+    // crossover on GB300: between T = 768 and 1024 at width 1152 (5 vectors
+    // per lane; the CTA-per-row form 4.5% faster at 768, 15% slower at 1024),
+    // T = 1536 at width 2048 (8 vectors per lane, fewer CTAs per SM)
     const int64_t lanes_vecs = ((int64_t)a.hidden / vec_elems<T>() + 31) / 32;
-    const bool ln_warp = a.rows >= (lanes_vecs <= 5 ? 5 : 10) * (int64_t)sms;
+    const bool ln_warp = a.rows >= (lanes_vecs <= 5 ? 6 : 10) * (int64_t)sms;
     if (vec && a.layernorm && v.nvec <= 256 && ln_warp) {
         // 4 rows per CTA: finer CTAs balance the last wave (measured on
         // GB300: 1.35x faster than 8 rows per CTA at T = 4096, width 1152)

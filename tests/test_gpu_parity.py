@@ -758,7 +758,7 @@ LN_CASES = {
     # one warp per row (<= 256 vectors, many rows): 1, 4, 5 and 8 vectors per
     # lane; several warps per row for few rows or longer rows
     "bf16_h256_T1000": dict(dtype=torch.bfloat16, T=1000, H=256, affine=True),
-    "f16_h1024_T800": dict(dtype=torch.float16, T=800, H=1024, affine=True),
+    "f16_h1024_T1000": dict(dtype=torch.float16, T=1000, H=1024, affine=True),
     "siglip_bf16_h1152_T1000": dict(dtype=torch.bfloat16, T=1000, H=1152, affine=True),
     "bf16_h2048_T1600_noaffine": dict(dtype=torch.bfloat16, T=1600, H=2048, affine=False),
     "f16_h640_T33": dict(dtype=torch.float16, T=33, H=640, affine=True),
@@ -796,7 +796,7 @@ def test_layernorm(name):
     run_ln(LN_CASES[name])
 
 
-@pytest.mark.parametrize("name", ["siglip_bf16_h1152_T512", "f16_h37_generic", "f16_h1024_T800",
+@pytest.mark.parametrize("name", ["siglip_bf16_h1152_T512", "f16_h37_generic", "f16_h1024_T1000",
                                   "siglip_bf16_h1152_T1000", "bf16_h4096_T300"])
 def test_layernorm_fp8_and_in_place(name):
     run_ln(LN_CASES[name], fp8=True)

@@ -41,6 +41,7 @@ import hashlib
 import json
 import os
 import platform
+import re
 import subprocess
 import sys
 import threading
@@ -567,14 +568,18 @@ def capture(torch, fn, stream):
 
 
 def source_sha(kernel):
-    """Hash of the source file that holds the kernel and of the shared device
-    helpers it includes, so that a stored capture goes stale whenever the
-    kernel's code may have changed."""
+    """Hash of the code of the source file that holds the kernel and of the
+    shared device helpers it includes, so that a stored capture goes stale
+    whenever the kernel's code may have changed.  Comments and whitespace are
+    left out: editing them changes no kernel."""
     csrc = os.path.join(ROOT, "memory_bound_decode_qk_gb300", "csrc")
     h = hashlib.sha256()
     for name in (OP_SOURCE[kernel], "edge_common.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -20,8 +20,9 @@
 // on GB300: the earlier form, which divided the thread index by a run-time
 // row width and looped over rows, took 1.79 us per decode-width launch at
 // T = 64 and 3.1 us at T = 512 against 1.57 and 2.2 us for this one.)  The
-// sum of squares is reduced with warp shuffles, and through shared memory
-// with one barrier when W > 1.  W and V come from the row length and the row
+// sum of squares is reduced with warp shuffles, then through shared memory
+// with one barrier.  The elementwise steps run on fp32 pairs (packed two-lane
+// instructions).  W and V come from the row length and the row
 // count: few rows spread over more warps, many rows favour more bytes in
 // flight per thread.  Rows whose length or alignment does not allow 16-byte
 // vectors take a scalar two-pass kernel: one CTA per row, and the second pass

@@ -25,6 +25,7 @@ from helpers import (TORCH_FMT, f32_ok, position_delta_bf16, report, storage, st
                      ulp_distance, within_one_ulp)
 from memory_bound_decode_qk_gb300 import edge_ops, synth
 from tolerances import ETA_NORM, REL_F32, gate_eta
+import case_stats
 
 pytestmark = pytest.mark.gpu
 
@@ -76,18 +77,29 @@ def calib_inv(pre):
     return float(np.float32(1.0) / np.float32(amax / 448.0))
 
 
+def _rel(value, exact, mag):
+    """|value - exact| over the magnitude scale (over |exact| where mag is 0)."""
+    scale = np.where(mag > 0, mag, np.maximum(np.abs(exact), 1e-300))
+    return np.abs(value - exact) / scale
+
+
 def check_dtype_out(name, got, ref_bits, lo, hi, mag, fmt, eta):
     """bf16/fp16: <= 1 ulp everywhere (at the pair norm for rotated channels)
     and the strict check."""
+    d = ulp_distance(got, ref_bits, fmt)
+    if case_stats.enabled():
+        case_stats.record(name, got, d, _rel(oracle.decode(got, fmt), lo, mag))
     one = within_one_ulp(got, ref_bits, mag, fmt)
     assert one.all(), report(name + " (1 ulp)", one)
-    d = ulp_distance(got, ref_bits, fmt)
     ok = strict_ok(got, lo, hi, mag, fmt, eta)
     assert ok.all(), report(name, ok)
     return float(np.mean(d == 0))
 
 
 def check_fp8_out(name, got, lo, hi, mag, eta, inv):
+    if case_stats.enabled():
+        d = ulp_distance(got, oracle.quantize(lo, inv), oracle.E4M3)
+        case_stats.record(name, got, d, _rel(oracle.decode(got, oracle.E4M3) / inv, lo, mag))
     ok = strict_ok(got, lo, hi, mag, oracle.E4M3, eta, inv_scale=inv)
     assert ok.all(), report(name, ok)
 
@@ -98,6 +110,9 @@ def check_out(name, got, ref_bits, pre, mag, fmt, out_fmt, eta, inv=1.0, lo=None
     if out_fmt == oracle.E4M3:
         check_fp8_out(name, got, lo, hi, mag, eta, inv)
     elif fmt == oracle.F32:
+        if case_stats.enabled():
+            d = ulp_distance(got, oracle.encode(pre, oracle.F32), oracle.F32)
+            case_stats.record(name, got, d, _rel(got.view(np.float32).astype(np.float64), pre, mag))
         ok = f32_ok(got, pre, mag, REL_F32)
         assert ok.all(), report(name, ok)
     else:
@@ -455,7 +470,10 @@ def run_rows(c, fused, fp8=False, inplace=False, seed=0):
     g.check()
     if gr is not None:
         gr.check()
-        assert np.array_equal(storage(gr.t.cpu()), ref_res), "residual sum not bit-exact"
+        res = storage(gr.t.cpu())
+        if case_stats.enabled():
+            case_stats.record("residual", res, ulp_distance(res, ref_res, fmt))
+        assert np.array_equal(res, ref_res), "residual sum not bit-exact"
     got = storage(g.t.cpu())
     check_out("out", got, ref_out, pre, np.abs(pre), fmt, out_fmt, ETA_NORM, inv)
 

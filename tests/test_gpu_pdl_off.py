@@ -34,6 +34,8 @@ def test_parity_cases_with_dependent_launch_off():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     env = dict(os.environ, EDGE_OPS_PDL="0")
+    # the child's cases would repeat the parent's lines in a stats dump
+    env.pop("EDGE_OPS_REPORT_STATS", None)
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(HERE, "test_gpu_parity.py"),
                         "-q", "-x", "-p", "no:cacheprovider", "-k", SELECT],
                        env=env, capture_output=True, text=True, timeout=1200)

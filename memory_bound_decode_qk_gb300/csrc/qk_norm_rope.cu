@@ -20,8 +20,11 @@
 //     before the dependent-launch wait.
 // Units are ordered token-major, so the warps of a CTA share cos/sin rows and
 // the norm weights.  Streamed inputs use evict-first loads.
-// Many heads: the four-threads-per-head path (qk_quad.cu) takes over past a
-// measured number of waves of this path's grid (quad_min_waves).
+// Mid widths, for 16-bit 512-byte rotate-half heads whose rotary channels
+// lie in the first half (the text profiles): the same layout with two
+// vectors per lane, 16 lanes per head.  Many heads: the four-threads-per-head
+// path (qk_quad.cu) takes over past a measured number of waves of this
+// path's grid (quad_min_waves; 1.6 for the heads with the two-vector form).
 // Generic path: one warp per head, staged through shared memory.  It serves
 // any head_dim up to 2048, any even rotary_dim and any element-aligned
 // pointer.
@@ -72,6 +75,115 @@ __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
     CacheRegs<T, LAYOUT> cr;
     if (role != 0) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
     qk_core<T, FP8, LPH, LAYOUT>(p, un.dst, active, lane, sub, raw, w, role, cr);
+}
+
+// Two vectors per lane, for mid widths: lane sub of an LPH-lane group holds
+// the head's vectors sub and sub + LPH, so a warp carries 32 / LPH heads of
+// 2 LPH vectors and every per-head step (address decoding, the position and
+// cache loads, the shuffle tree, the partner shuffle) serves twice the data
+// of the one-vector form.  Rotate-half heads whose rotary channels all lie in
+// the first LPH vectors, in the rounded mode: the second vector of a lane
+// never rotates.  The arithmetic is qk_core's, on fp32 pairs.
+template <typename T, bool FP8, int LPH>
+__global__ void __launch_bounds__(256) qk_vec2_kernel(QKP p) {
+    constexpr int N = vec_elems<T>();
+    constexpr int P = N / 2;
+    constexpr int HPW = 32 / LPH;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (LPH - 1);
+    // < 2^31 + 8 HPW: units are at most 2^31 - 1 (validated)
+    const uint32_t u = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * HPW + lane / LPH;
+    const bool active = u < p.units;
+    const Unit un = locate(p, active ? u : 0);
+
+    if (threadIdx.x == 0) {
+        const uint32_t per_cta = (blockDim.x >> 5) * HPW;
+        prefetch_heads(p, blockIdx.x * per_cta, (blockIdx.x + 1) * per_cta, true);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int lane_role = p.rot > 0 ? rotary_role<T, kRotateHalf>(p, sub) : 0;
+    uint4 raw0 = make_uint4(0u, 0u, 0u, 0u), raw1 = raw0;
+    int64_t pos = -1;
+    if (active) {
+        raw0 = __ldcs(reinterpret_cast<const uint4*>(un.src) + sub);
+        raw1 = __ldcs(reinterpret_cast<const uint4*>(un.src) + sub + LPH);
+        if (p.rot > 0) pos = __ldg(p.pos + un.t);
+    }
+    float w0[N], w1[N];
+    weights_plus_delta<T>(p, un.w, sub, w0);
+    weights_plus_delta<T>(p, un.w, sub + LPH, w1);
+    const bool rot = active && pos >= 0 && pos < p.cache_len;
+    const int role = rot ? lane_role : 0;
+    CacheRegs<T, kRotateHalf> cr;
+    if (role != 0) load_cache<T, kRotateHalf>(p, pos, sub, role, cr);
+
+    // normalized values n (x itself without normalization), rounded to the
+    // dtype as `mine` (first vector) and `mine1` (second)
+    float2 x0[P], x1[P], n0[P], n1[P];
+    unpack_pairs<T, N>(raw0, x0);
+    unpack_pairs<T, N>(raw1, x1);
+    if (p.mode & kModeNorm) {
+        float2 s2 = splat2(0.0f);
+#pragma unroll
+        for (int j = 0; j < P; ++j) s2 = __ffma2_rn(x0[j], x0[j], s2);
+#pragma unroll
+        for (int j = 0; j < P; ++j) s2 = __ffma2_rn(x1[j], x1[j], s2);
+        const float ss = group_sum<LPH>(__fadd_rn(s2.x, s2.y));
+        const float2 r2 = splat2(inv_rms(ss, p.invD, p.eps));
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            n0[j] = __fmul2_rn(__fmul2_rn(x0[j], r2), make_float2(w0[2 * j], w0[2 * j + 1]));
+            n1[j] = __fmul2_rn(__fmul2_rn(x1[j], r2), make_float2(w1[2 * j], w1[2 * j + 1]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            n0[j] = x0[j];
+            n1[j] = x1[j];
+        }
+    }
+    const uint4 mine = pack_pairs<T, N>(n0);
+    const uint4 mine1 = pack_pairs<T, N>(n1);
+    float2 m[P], y[P];
+    unpack_pairs<T, N>(mine, m);
+#pragma unroll
+    for (int j = 0; j < P; ++j) y[j] = m[j];
+
+    // rotate-half on the first vector: the partner is half/N lanes away
+    const int hv = p.half / N;
+    const int from = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
+    uint4 other;
+    other.x = __shfl_sync(0xffffffffu, mine.x, from);
+    other.y = __shfl_sync(0xffffffffu, mine.y, from);
+    other.z = __shfl_sync(0xffffffffu, mine.z, from);
+    other.w = __shfl_sync(0xffffffffu, mine.w, from);
+    float2 pm[P];
+    unpack_pairs<T, N>(other, pm);
+    if (role != 0) {
+        // first member: x c - x' s; second: x c + x' s (the sine's sign
+        // folded into the product, which rounds symmetrically)
+        const float sg = role == 1 ? -1.0f : 1.0f;
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            const float2 sn = make_float2(sg * cr.s[2 * j], sg * cr.s[2 * j + 1]);
+            y[j] = __ffma2_rn(m[j], make_float2(cr.c[2 * j], cr.c[2 * j + 1]), __fmul2_rn(pm[j], sn));
+        }
+    }
+    if (active) {
+        if constexpr (FP8) {
+            float2 m1[P];
+            unpack_pairs<T, N>(mine1, m1);
+            auto q0 = quantize_pairs<N>(y, p.inv);
+            auto q1 = quantize_pairs<N>(m1, p.inv);
+            reinterpret_cast<decltype(q0)*>(un.dst)[sub] = q0;
+            reinterpret_cast<decltype(q1)*>(un.dst)[sub + LPH] = q1;
+        } else {
+            reinterpret_cast<uint4*>(un.dst)[sub] = pack_pairs<T, N>(y);
+            reinterpret_cast<uint4*>(un.dst)[sub + LPH] = mine1;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- generic path
@@ -159,10 +271,33 @@ cudaError_t launch_typed(const QKArgs& a, QKP& p, cudaStream_t s) {
         const int64_t hbytes = (int64_t)D * (int64_t)sizeof(T);
         const double wave = (double)resident_ctas((const void*)vfn, threads) * sms *
                             quad_min_waves((int)sizeof(T), a.layout, a.rotary_dim, hbytes);
-        if ((double)blocks > wave && quad_suits(a.layout, a.rotary_dim, hbytes)) {
+        // 16-bit heads of 512 bytes whose rotary channels lie in the first
+        // half (the text profiles), in the rounded mode, have a third form:
+        // two vectors per lane.  Measured on GB300 against both others over
+        // T = 1 to 1024 for the (16,2) and (24,4) text profiles and RoPE
+        // alone, in units of the one-vector grid's waves w: the one-vector
+        // form wins for w <= 0.25 (by up to 4%) and at 0.8 < w <= 1, where it
+        // fills one balanced wave (by 6-8%); two vectors win elsewhere up to
+        // w = 1.6 (by 8-18%, over four threads per head from w = 1); four
+        // threads per head beyond.
+        const bool two = sizeof(T) == 2 && hbytes == 512 && a.layout == kRotateHalf &&
+                         a.rotary_dim <= D / 2 && (a.mode & kModeUnrounded) == 0;
+        const double w = (double)blocks / (double)(resident_ctas((const void*)vfn, threads) * sms);
+        const bool take_quad = two ? w > 1.6 : (double)blocks > wave;
+        if (take_quad && quad_suits(a.layout, a.rotary_dim, hbytes)) {
             bool handled = false;
             cudaError_t e = launch_qk_quad<T, FP8>(a, p, cfg, &handled);
             if (handled || e != cudaSuccess) return e;
+        }
+        if constexpr (sizeof(T) == 2) {
+            if (two && w > 0.25 && !(w > 0.8 && w <= 1.0)) {
+                // 16 lanes per head, two heads per warp, 16 heads per CTA
+                const int64_t per2 = (int64_t)(threads / 32) * 2;
+                cfg.gridDim = dim3((unsigned)(((int64_t)p.units + per2 - 1) / per2));
+                cfg.blockDim = dim3(threads);
+                cfg.dynamicSmemBytes = 0;
+                return cudaLaunchKernelEx(&cfg, qk_vec2_kernel<T, FP8, 16>, p);
+            }
         }
         // one-shot: units <= 2^31 - 1 (validated), so blocks < 2^28
         cfg.gridDim = dim3((unsigned)blocks);

@@ -203,7 +203,16 @@ QK_CASES = {
     "quad_no_rotation": dict(dtype=torch.float16, T=800, Hq=24, Hk=4, D=256, rot=0, layout=0,
                              w_mean=0.0, w_std=0.1, offset=1, theta=1e4, P=16,
                              positions="arange"),
-    # rotary width whose pairs are not thread-local: the lane-group path serves it
+    # mid widths of 16-bit 512-byte heads: two vectors per lane (the grid at
+    # 0.44 and 1.38 of a one-vector wave), with tokens past the cache
+    "two_vec_16_2_T150": dict(dtype=torch.bfloat16, T=150, Hq=16, Hk=2, D=256, rot=64, layout=0,
+                              w_mean=0.0, w_std=0.05, offset=1, theta=1e7, P=100,
+                              positions="arange"),
+    "two_vec_f16_24_4_T300": dict(dtype=torch.float16, T=300, Hq=24, Hk=4, D=256, rot=128,
+                                  layout=0, w_mean=1.0, w_std=0.02, offset=0, theta=1e6, P=4096,
+                                  positions="arange"),
+    # rotary width whose pairs are not thread-local for four threads per head:
+    # the lane-group path serves it (two vectors per lane at this width)
     "quad_declined_rot32": dict(dtype=torch.bfloat16, T=800, Hq=24, Hk=4, D=256, rot=32,
                                 layout=0, w_mean=0.0, w_std=0.05, offset=1, theta=1e7,
                                 P=32768, positions="offset"),
@@ -266,6 +275,7 @@ def test_qk_norm_rope(name):
 
 
 @pytest.mark.parametrize("name", ["cfg3_16_2_T333", "cfg3_24_4_T8", "cfg4_bf16", "cfg1_f32",
+                                  "two_vec_16_2_T150", "two_vec_f16_24_4_T300",
                                   "generic_odd_d37", "d128_bf16", "quad_f32_d128",
                                   "quad_f16_d64_interleaved", "quad_cfg4_interleaved",
                                   "dflash2_W16_B32"])
@@ -332,9 +342,11 @@ def test_qk_without_cache_rows_rotates_nothing(T):
 
 # Geometries of the lane-group prologue under a position rewrite: one head per
 # warp (bf16, 256), two heads per warp (bf16, 128), fp32 heads (one per warp,
-# four channels per lane) and the interleaved cache load.
+# four channels per lane), the interleaved cache load, and enough heads for
+# the two-vectors-per-lane form (12 tokens of 136 heads: 0.27 of a wave).
 REWRITE_GEOMS = {
     "bf16_d256_rot64": (torch.bfloat16, 16, 2, 256, 64, 0),
+    "bf16_d256_rot64_two_vectors": (torch.bfloat16, 128, 8, 256, 64, 0),
     "bf16_d128_rot128": (torch.bfloat16, 8, 2, 128, 128, 0),
     "f32_d128_rot64": (torch.float32, 4, 2, 128, 64, 0),
     "bf16_d256_interleaved": (torch.bfloat16, 8, 2, 256, 256, 1),
@@ -675,6 +687,8 @@ ROPE_CASES = {
                                  P=4096, positions="cfg_out_of_cache"),
     "many_heads_bf16": dict(dtype=torch.bfloat16, T=900, Hq=24, Hk=4, D=256, rot=64, layout=0,
                             P=32768, positions="offset"),
+    "mid_heads_two_vectors": dict(dtype=torch.bfloat16, T=128, Hq=24, Hk=4, D=256, rot=64,
+                                  layout=0, P=32768, positions="offset"),
     "many_heads_interleaved": dict(dtype=torch.bfloat16, T=1000, Hq=16, Hk=8, D=256, rot=256,
                                    layout=1, P=4096, positions="arange"),
     "generic_d96": dict(dtype=torch.bfloat16, T=9, Hq=3, Hk=1, D=96, rot=40, layout=0, P=16,
@@ -719,7 +733,7 @@ def test_rope(name):
 
 
 @pytest.mark.parametrize("name", ["bf16_partial_rotate_half", "many_heads_interleaved",
-                                  "f32_full_rotate_half"])
+                                  "f32_full_rotate_half", "mid_heads_two_vectors"])
 def test_rope_fp8(name):
     run_rope(ROPE_CASES[name], fp8=True)
 

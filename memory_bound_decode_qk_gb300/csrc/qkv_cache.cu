@@ -17,7 +17,9 @@
 // one 16-byte vector per lane of an LPH-lane group, and a one-shot grid puts
 // every head in flight, the regime of decode widths.  Units are token-major
 // over the Hq + 2 Hk heads of a row.  A v head rides the same code with no
-// norm and no rotation, so a warp never diverges around the shuffles.
+// norm and no rotation, so a warp never diverges around the shuffles.  Mid
+// widths of the text-profile heads take two vectors per lane, and many
+// heads four threads per head (qk_quad.cu), as in the prologue.
 #include "qk_common.cuh"
 
 namespace edge {
@@ -77,6 +79,122 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
     if (role != 0) load_cache<T, LAYOUT>(p, pos, sub, role, cr);
     qk_core<T, false, LPH, LAYOUT>(p, dst, active && dst != nullptr, lane, sub, raw, w, role, cr,
                                    isv);
+}
+
+// Two vectors per lane for mid widths, as in the prologue: lane sub of a
+// 16-lane group holds vectors sub and sub + LPH of one head, two heads per
+// warp.  Rotate-half heads whose rotary channels lie in the first LPH
+// vectors; a v head is copied exactly (no norm, no rotation).  Held to 64
+// registers: 4 CTAs of 256 threads per SM, as the prologue's form.
+template <typename T, int LPH>
+__global__ void __launch_bounds__(256, 4) qkv_vec2_kernel(QKVP a) {
+    constexpr int N = vec_elems<T>();
+    constexpr int P = N / 2;
+    constexpr int HPW = 32 / LPH;
+    const QKP& p = a.p;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (LPH - 1);
+    const int hb = p.D * (int)sizeof(T);
+    // one-shot grid; < 2^31 + 8 HPW since units are at most 2^31 - 1
+    const uint32_t u = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * HPW + lane / LPH;
+    const bool active = u < p.units;
+    const uint32_t t = fast_div(active ? u : 0, a.per_token);
+    const int h = (int)((active ? u : 0) - t * a.per_token.d);
+    const char* src = p.q + (int64_t)t * a.row_bytes + (int64_t)h * hb;
+    const bool isq = h < p.q_heads;
+    const bool isv = h >= p.q_heads + p.k_heads;
+    const int j = isq ? h : (isv ? h - p.q_heads - p.k_heads : h - p.q_heads);
+
+    if (threadIdx.x == 0) {
+        const uint32_t per_cta = (blockDim.x >> 5) * HPW;
+        const uint32_t u0 = blockIdx.x * per_cta;
+        const uint32_t u1 = u0 + per_cta < p.units ? u0 + per_cta : p.units;
+        if (u0 < u1) {
+            const int64_t t0 = fast_div(u0, a.per_token), t1 = fast_div(u1 - 1, a.per_token) + 1;
+            prefetch_l2(p.q, t0 * a.row_bytes, t1 * a.row_bytes);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int lane_role = p.rot > 0 ? rotary_role<T, kRotateHalf>(p, sub) : 0;
+    uint4 raw0 = make_uint4(0u, 0u, 0u, 0u), raw1 = raw0;
+    int64_t pos = -1, slot = -1;
+    if (active) {
+        raw0 = __ldcs(reinterpret_cast<const uint4*>(src) + sub);
+        raw1 = __ldcs(reinterpret_cast<const uint4*>(src) + sub + LPH);
+        if (p.rot > 0 && !isv) pos = __ldg(p.pos + t);
+        if (!isq && a.slots != nullptr) slot = __ldg(a.slots + t);
+    }
+    char* dst = nullptr;
+    if (isq) {
+        dst = p.qo + ((int64_t)t * p.q_heads + j) * hb;
+    } else if (slot >= 0 && slot < a.num_slots) {
+        dst = (isv ? a.vc : a.kc) + (slot * p.k_heads + j) * hb;
+    }
+    float w0[N], w1[N];
+    weights_plus_delta<T>(p, isq ? p.wq : p.wk, sub, w0);
+    weights_plus_delta<T>(p, isq ? p.wq : p.wk, sub + LPH, w1);
+    const bool rot = active && !isv && pos >= 0 && pos < p.cache_len;
+    const int role = rot ? lane_role : 0;
+    CacheRegs<T, kRotateHalf> cr;
+    if (role != 0) load_cache<T, kRotateHalf>(p, pos, sub, role, cr);
+
+    float2 x0[P], x1[P], n0[P], n1[P];
+    unpack_pairs<T, N>(raw0, x0);
+    unpack_pairs<T, N>(raw1, x1);
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+        n0[q] = x0[q];
+        n1[q] = x1[q];
+    }
+    if (p.mode & kModeNorm) {
+        // every lane group joins the shuffle tree; a v head keeps x
+        float2 s2 = splat2(0.0f);
+#pragma unroll
+        for (int q = 0; q < P; ++q) s2 = __ffma2_rn(x0[q], x0[q], s2);
+#pragma unroll
+        for (int q = 0; q < P; ++q) s2 = __ffma2_rn(x1[q], x1[q], s2);
+        const float ss = group_sum<LPH>(__fadd_rn(s2.x, s2.y));
+        const float2 r2 = splat2(inv_rms(ss, p.invD, p.eps));
+        if (!isv) {
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                n0[q] = __fmul2_rn(__fmul2_rn(x0[q], r2), make_float2(w0[2 * q], w0[2 * q + 1]));
+                n1[q] = __fmul2_rn(__fmul2_rn(x1[q], r2), make_float2(w1[2 * q], w1[2 * q + 1]));
+            }
+        }
+    }
+    // a v head's values are already in the dtype, so these packs copy its
+    // bits exactly
+    const uint4 mine = pack_pairs<T, N>(n0);
+    const uint4 mine1 = pack_pairs<T, N>(n1);
+    float2 m[P], y[P];
+    unpack_pairs<T, N>(mine, m);
+#pragma unroll
+    for (int q = 0; q < P; ++q) y[q] = m[q];
+
+    const int hv = p.half / N;
+    const int from = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
+    uint4 other;
+    other.x = __shfl_sync(0xffffffffu, mine.x, from);
+    other.y = __shfl_sync(0xffffffffu, mine.y, from);
+    other.z = __shfl_sync(0xffffffffu, mine.z, from);
+    other.w = __shfl_sync(0xffffffffu, mine.w, from);
+    float2 pm[P];
+    unpack_pairs<T, N>(other, pm);
+    if (role != 0) {
+        const float sg = role == 1 ? -1.0f : 1.0f;
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+            const float2 sn = make_float2(sg * cr.s[2 * q], sg * cr.s[2 * q + 1]);
+            y[q] = __ffma2_rn(m[q], make_float2(cr.c[2 * q], cr.c[2 * q + 1]), __fmul2_rn(pm[q], sn));
+        }
+    }
+    if (active && dst != nullptr) {
+        reinterpret_cast<uint4*>(dst)[sub] = role != 0 ? pack_pairs<T, N>(y) : mine;
+        reinterpret_cast<uint4*>(dst)[sub + LPH] = mine1;
+    }
 }
 
 // Any head size or alignment: one warp per head, staged in shared memory.
@@ -186,12 +304,29 @@ cudaError_t launch_typed(const QKVArgs& a, QKVP& k, cudaStream_t s, bool* handle
     const int64_t per_block = (int64_t)(threads / 32) * hpw;
     int64_t blocks = ((int64_t)k.p.units + per_block - 1) / per_block;
     // the prologue's rule: the one-shot lane-group grid while it fits in one
-    // wave of resident CTAs, four threads per head beyond
+    // wave of resident CTAs, four threads per head beyond; for 16-bit
+    // rotate-half heads of 512 bytes whose rotary channels lie in the first
+    // half, the prologue's three bands in waves w of the one-vector grid
+    // (one vector to 0.25 and from 0.8 to 1, two vectors elsewhere up to 1.6,
+    // four threads per head beyond)
     const int64_t wave = (int64_t)resident_ctas((const void*)vfn, threads) * sm_count();
-    if (blocks > wave && quad_suits(a.layout, k.p.rot, (int64_t)D * (int64_t)sizeof(T))) {
+    const bool two = sizeof(T) == 2 && D * (int)sizeof(T) == 512 && a.layout == kRotateHalf &&
+                     k.p.rot <= D / 2;
+    const double w = (double)blocks / (double)wave;
+    const bool take_quad = two ? w > 1.6 : blocks > wave;
+    if (take_quad && quad_suits(a.layout, k.p.rot, (int64_t)D * (int64_t)sizeof(T))) {
         bool quad = false;
         cudaError_t e = launch_qkv_quad<T>(a, k, cfg, &quad);
         if (quad || e != cudaSuccess) return e;
+    }
+    if constexpr (sizeof(T) == 2) {
+        if (two && w > 0.25 && !(w > 0.8 && w <= 1.0)) {
+            const int64_t per2 = (int64_t)(threads / 32) * 2;
+            cfg.gridDim = dim3((unsigned)(((int64_t)k.p.units + per2 - 1) / per2));
+            cfg.blockDim = dim3(threads);
+            cfg.dynamicSmemBytes = 0;
+            return cudaLaunchKernelEx(&cfg, qkv_vec2_kernel<T, 16>, k);
+        }
     }
     cfg.gridDim = dim3((unsigned)blocks);  // one-shot: blocks < 2^28
     cfg.blockDim = dim3(threads);

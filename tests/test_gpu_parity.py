@@ -870,6 +870,12 @@ QKV_CASES = {
                       offset=1, S=4),
     "prefill_T2000": dict(dtype=torch.bfloat16, T=2000, Hq=16, Hk=2, D=256, rot=64, layout=0,
                           norm=True, offset=1, S=2048),
+    # mid widths of the text-profile heads: two vectors per lane (0.49 and 1.32
+    # of a one-vector wave)
+    "two_vec_text_T150": dict(dtype=torch.bfloat16, T=150, Hq=16, Hk=2, D=256, rot=64, layout=0,
+                              norm=True, offset=1, S=256),
+    "two_vec_f16_no_norm_T400": dict(dtype=torch.float16, T=400, Hq=16, Hk=2, D=256, rot=128,
+                                     layout=0, norm=False, offset=0, S=512),
     # many heads (the lane-group grid is over a wave): four threads per head
     "quad_qwen_d128_T1000": dict(dtype=torch.bfloat16, T=1000, Hq=32, Hk=8, D=128, rot=128,
                                  layout=0, norm=True, offset=0, S=1024),

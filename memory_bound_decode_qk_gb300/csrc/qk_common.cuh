@@ -263,6 +263,90 @@ __device__ __forceinline__ void weights_plus_delta(const QKP& p, const char* wpt
     }
 }
 
+// qk_core for a head held as two 16-byte vectors per lane of an LPH-lane
+// group: vectors sub (raw0, weights w0) and sub + LPH (raw1, w1).  Rotate-half
+// heads whose rotary channels all lie in the first LPH vectors, in the
+// rounded mode, so only the first vector rotates (partner over the same
+// shuffle as qk_core).  All 32 lanes of the warp call this together.
+//  copy: pass the head through unnormalized and unrotated (the v heads of the
+//  fused QKV op); the lane group still joins the warp-wide reduction.
+template <typename T, bool FP8, int LPH>
+__device__ __forceinline__ void qk_core2(const QKP& p, char* dst, bool active, int lane, int sub,
+                                         const uint4& raw0, const uint4& raw1,
+                                         const float (&w0)[vec_elems<T>()],
+                                         const float (&w1)[vec_elems<T>()], int role,
+                                         const CacheRegs<T, kRotateHalf>& cr, bool copy = false) {
+    constexpr int N = vec_elems<T>();
+    constexpr int P = N / 2;
+    // normalized values n (x itself without normalization or for a copy),
+    // rounded to the dtype as `mine` (first vector) and `mine1` (second); the
+    // values of a copy are already in the dtype, so its packs are exact
+    float2 x0[P], x1[P], n0[P], n1[P];
+    unpack_pairs<T, N>(raw0, x0);
+    unpack_pairs<T, N>(raw1, x1);
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+        n0[j] = x0[j];
+        n1[j] = x1[j];
+    }
+    if (p.mode & kModeNorm) {
+        float2 s2 = splat2(0.0f);
+#pragma unroll
+        for (int j = 0; j < P; ++j) s2 = __ffma2_rn(x0[j], x0[j], s2);
+#pragma unroll
+        for (int j = 0; j < P; ++j) s2 = __ffma2_rn(x1[j], x1[j], s2);
+        const float ss = group_sum<LPH>(__fadd_rn(s2.x, s2.y));
+        const float2 r2 = splat2(inv_rms(ss, p.invD, p.eps));
+        if (!copy) {
+#pragma unroll
+            for (int j = 0; j < P; ++j) {
+                n0[j] = __fmul2_rn(__fmul2_rn(x0[j], r2), make_float2(w0[2 * j], w0[2 * j + 1]));
+                n1[j] = __fmul2_rn(__fmul2_rn(x1[j], r2), make_float2(w1[2 * j], w1[2 * j + 1]));
+            }
+        }
+    }
+    const uint4 mine = pack_pairs<T, N>(n0);
+    const uint4 mine1 = pack_pairs<T, N>(n1);
+    float2 m[P], y[P];
+    unpack_pairs<T, N>(mine, m);
+#pragma unroll
+    for (int j = 0; j < P; ++j) y[j] = m[j];
+
+    // rotate-half on the first vector: the partner is half/N lanes away
+    const int hv = p.half / N;
+    const int from = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
+    uint4 other;
+    other.x = __shfl_sync(0xffffffffu, mine.x, from);
+    other.y = __shfl_sync(0xffffffffu, mine.y, from);
+    other.z = __shfl_sync(0xffffffffu, mine.z, from);
+    other.w = __shfl_sync(0xffffffffu, mine.w, from);
+    float2 pm[P];
+    unpack_pairs<T, N>(other, pm);
+    if (role != 0) {
+        // first member: x c - x' s; second: x c + x' s (the sine's sign
+        // folded into the product, which rounds symmetrically)
+        const float sg = role == 1 ? -1.0f : 1.0f;
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            const float2 sn = make_float2(sg * cr.s[2 * j], sg * cr.s[2 * j + 1]);
+            y[j] = __ffma2_rn(m[j], make_float2(cr.c[2 * j], cr.c[2 * j + 1]), __fmul2_rn(pm[j], sn));
+        }
+    }
+    if (active) {
+        if constexpr (FP8) {
+            float2 m1[P];
+            unpack_pairs<T, N>(mine1, m1);
+            auto q0 = quantize_pairs<N>(y, p.inv);
+            auto q1 = quantize_pairs<N>(m1, p.inv);
+            reinterpret_cast<decltype(q0)*>(dst)[sub] = q0;
+            reinterpret_cast<decltype(q1)*>(dst)[sub + LPH] = q1;
+        } else {
+            reinterpret_cast<uint4*>(dst)[sub] = role != 0 ? pack_pairs<T, N>(y) : mine;
+            reinterpret_cast<uint4*>(dst)[sub + LPH] = mine1;
+        }
+    }
+}
+
 // Threads-per-head path for many heads (qk_quad.cu).  *handled is false when
 // the geometry is outside its instantiations; the caller then takes the
 // lane-group path.

@@ -83,11 +83,10 @@ __global__ void __launch_bounds__(256) qk_vec_kernel(QKP p) {
 // cache loads, the shuffle tree, the partner shuffle) serves twice the data
 // of the one-vector form.  Rotate-half heads whose rotary channels all lie in
 // the first LPH vectors, in the rounded mode: the second vector of a lane
-// never rotates.  The arithmetic is qk_core's, on fp32 pairs.
+// never rotates (qk_core2).
 template <typename T, bool FP8, int LPH>
 __global__ void __launch_bounds__(256) qk_vec2_kernel(QKP p) {
     constexpr int N = vec_elems<T>();
-    constexpr int P = N / 2;
     constexpr int HPW = 32 / LPH;
     const int lane = threadIdx.x & 31;
     const int sub = lane & (LPH - 1);
@@ -119,71 +118,7 @@ __global__ void __launch_bounds__(256) qk_vec2_kernel(QKP p) {
     CacheRegs<T, kRotateHalf> cr;
     if (role != 0) load_cache<T, kRotateHalf>(p, pos, sub, role, cr);
 
-    // normalized values n (x itself without normalization), rounded to the
-    // dtype as `mine` (first vector) and `mine1` (second)
-    float2 x0[P], x1[P], n0[P], n1[P];
-    unpack_pairs<T, N>(raw0, x0);
-    unpack_pairs<T, N>(raw1, x1);
-    if (p.mode & kModeNorm) {
-        float2 s2 = splat2(0.0f);
-#pragma unroll
-        for (int j = 0; j < P; ++j) s2 = __ffma2_rn(x0[j], x0[j], s2);
-#pragma unroll
-        for (int j = 0; j < P; ++j) s2 = __ffma2_rn(x1[j], x1[j], s2);
-        const float ss = group_sum<LPH>(__fadd_rn(s2.x, s2.y));
-        const float2 r2 = splat2(inv_rms(ss, p.invD, p.eps));
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-            n0[j] = __fmul2_rn(__fmul2_rn(x0[j], r2), make_float2(w0[2 * j], w0[2 * j + 1]));
-            n1[j] = __fmul2_rn(__fmul2_rn(x1[j], r2), make_float2(w1[2 * j], w1[2 * j + 1]));
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-            n0[j] = x0[j];
-            n1[j] = x1[j];
-        }
-    }
-    const uint4 mine = pack_pairs<T, N>(n0);
-    const uint4 mine1 = pack_pairs<T, N>(n1);
-    float2 m[P], y[P];
-    unpack_pairs<T, N>(mine, m);
-#pragma unroll
-    for (int j = 0; j < P; ++j) y[j] = m[j];
-
-    // rotate-half on the first vector: the partner is half/N lanes away
-    const int hv = p.half / N;
-    const int from = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
-    uint4 other;
-    other.x = __shfl_sync(0xffffffffu, mine.x, from);
-    other.y = __shfl_sync(0xffffffffu, mine.y, from);
-    other.z = __shfl_sync(0xffffffffu, mine.z, from);
-    other.w = __shfl_sync(0xffffffffu, mine.w, from);
-    float2 pm[P];
-    unpack_pairs<T, N>(other, pm);
-    if (role != 0) {
-        // first member: x c - x' s; second: x c + x' s (the sine's sign
-        // folded into the product, which rounds symmetrically)
-        const float sg = role == 1 ? -1.0f : 1.0f;
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-            const float2 sn = make_float2(sg * cr.s[2 * j], sg * cr.s[2 * j + 1]);
-            y[j] = __ffma2_rn(m[j], make_float2(cr.c[2 * j], cr.c[2 * j + 1]), __fmul2_rn(pm[j], sn));
-        }
-    }
-    if (active) {
-        if constexpr (FP8) {
-            float2 m1[P];
-            unpack_pairs<T, N>(mine1, m1);
-            auto q0 = quantize_pairs<N>(y, p.inv);
-            auto q1 = quantize_pairs<N>(m1, p.inv);
-            reinterpret_cast<decltype(q0)*>(un.dst)[sub] = q0;
-            reinterpret_cast<decltype(q1)*>(un.dst)[sub + LPH] = q1;
-        } else {
-            reinterpret_cast<uint4*>(un.dst)[sub] = pack_pairs<T, N>(y);
-            reinterpret_cast<uint4*>(un.dst)[sub + LPH] = mine1;
-        }
-    }
+    qk_core2<T, FP8, LPH>(p, un.dst, active, lane, sub, raw0, raw1, w0, w1, role, cr);
 }
 
 // ---------------------------------------------------------------- generic path

@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(256) qkv_vec_kernel(QKVP a) {
 template <typename T, int LPH>
 __global__ void __launch_bounds__(256, 4) qkv_vec2_kernel(QKVP a) {
     constexpr int N = vec_elems<T>();
-    constexpr int P = N / 2;
     constexpr int HPW = 32 / LPH;
     const QKP& p = a.p;
     const int lane = threadIdx.x & 31;
@@ -140,61 +139,8 @@ __global__ void __launch_bounds__(256, 4) qkv_vec2_kernel(QKVP a) {
     CacheRegs<T, kRotateHalf> cr;
     if (role != 0) load_cache<T, kRotateHalf>(p, pos, sub, role, cr);
 
-    float2 x0[P], x1[P], n0[P], n1[P];
-    unpack_pairs<T, N>(raw0, x0);
-    unpack_pairs<T, N>(raw1, x1);
-#pragma unroll
-    for (int q = 0; q < P; ++q) {
-        n0[q] = x0[q];
-        n1[q] = x1[q];
-    }
-    if (p.mode & kModeNorm) {
-        // every lane group joins the shuffle tree; a v head keeps x
-        float2 s2 = splat2(0.0f);
-#pragma unroll
-        for (int q = 0; q < P; ++q) s2 = __ffma2_rn(x0[q], x0[q], s2);
-#pragma unroll
-        for (int q = 0; q < P; ++q) s2 = __ffma2_rn(x1[q], x1[q], s2);
-        const float ss = group_sum<LPH>(__fadd_rn(s2.x, s2.y));
-        const float2 r2 = splat2(inv_rms(ss, p.invD, p.eps));
-        if (!isv) {
-#pragma unroll
-            for (int q = 0; q < P; ++q) {
-                n0[q] = __fmul2_rn(__fmul2_rn(x0[q], r2), make_float2(w0[2 * q], w0[2 * q + 1]));
-                n1[q] = __fmul2_rn(__fmul2_rn(x1[q], r2), make_float2(w1[2 * q], w1[2 * q + 1]));
-            }
-        }
-    }
-    // a v head's values are already in the dtype, so these packs copy its
-    // bits exactly
-    const uint4 mine = pack_pairs<T, N>(n0);
-    const uint4 mine1 = pack_pairs<T, N>(n1);
-    float2 m[P], y[P];
-    unpack_pairs<T, N>(mine, m);
-#pragma unroll
-    for (int q = 0; q < P; ++q) y[q] = m[q];
-
-    const int hv = p.half / N;
-    const int from = role == 1 ? lane + hv : (role == 2 ? lane - hv : lane);
-    uint4 other;
-    other.x = __shfl_sync(0xffffffffu, mine.x, from);
-    other.y = __shfl_sync(0xffffffffu, mine.y, from);
-    other.z = __shfl_sync(0xffffffffu, mine.z, from);
-    other.w = __shfl_sync(0xffffffffu, mine.w, from);
-    float2 pm[P];
-    unpack_pairs<T, N>(other, pm);
-    if (role != 0) {
-        const float sg = role == 1 ? -1.0f : 1.0f;
-#pragma unroll
-        for (int q = 0; q < P; ++q) {
-            const float2 sn = make_float2(sg * cr.s[2 * q], sg * cr.s[2 * q + 1]);
-            y[q] = __ffma2_rn(m[q], make_float2(cr.c[2 * q], cr.c[2 * q + 1]), __fmul2_rn(pm[q], sn));
-        }
-    }
-    if (active && dst != nullptr) {
-        reinterpret_cast<uint4*>(dst)[sub] = role != 0 ? pack_pairs<T, N>(y) : mine;
-        reinterpret_cast<uint4*>(dst)[sub + LPH] = mine1;
-    }
+    qk_core2<T, false, LPH>(p, dst, active && dst != nullptr, lane, sub, raw0, raw1, w0, w1, role,
+                            cr, isv);
 }
 
 // Any head size or alignment: one warp per head, staged in shared memory.
